@@ -19,6 +19,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -32,6 +33,7 @@ if ROOT not in sys.path:
 
 METRIC = "HBM GB/s (read+write) and % of GB300 peak, fused RMSNorm+MXFP8 quant"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "fused_rmsnorm_quant_32768x8192.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "mxfp8_block_scaled_rmsnorm_gb300", "csrc", f)
                   for f in ("mxfp8_kernels.cu", "mx_table.h")]
@@ -221,14 +223,39 @@ def cpu_cores() -> int:
     return len(os.sched_getaffinity(0))
 
 
-def time_oracle(t, rows: int, rowwise=True, columnwise=True):
-    """Wall time of the oracle's fused map on the first ``rows`` rows."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    fields = {}
+    try:
+        for line in open("/proc/cpuinfo"):
+            if ":" in line:
+                k, v = (p.strip() for p in line.split(":", 1))
+                fields.setdefault(k, v)
+    except OSError:
+        return "unknown"
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU implementer" in fields:
+        return f"implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    return "unknown"
+
+
+def time_oracle(t, rows: int, rowwise=True, columnwise=True, threads=None):
+    """Wall time of the oracle's fused map on the first ``rows`` rows, on
+    ``threads`` host threads (all cores of this process by default)."""
     import numpy as np
     import oracle
     x = np.ascontiguousarray(t.x[:rows])
     t0 = time.perf_counter()
     oracle.rmsnorm_quant_mxfp8(x, t.gamma, t.eps, t.offset, rowwise, columnwise,
-                               threads=cpu_cores())
+                               threads=threads or cpu_cores())
     return time.perf_counter() - t0
 
 
@@ -353,7 +380,8 @@ def run_reference(args, world, rank):
         "value": value,
         "ms_per_step": per_step * 1e3,
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cpu_cores(),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "cpu_model": cpu_model(),
+                         "arch": platform.machine()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -643,9 +671,17 @@ def main():
         rows = min(R, max(32, args.cpu_rows // 32 * 32))
         el = time_oracle(t, rows, wl.rowwise, wl.columnwise)
         sb = W.algorithmic_bytes(rows, C, True, wl.rowwise, wl.columnwise)
+        # one thread on an eighth of the rows (the same per-row work)
+        rows1 = min(rows, max(32, rows // 8 // 32 * 32))
+        el1 = time_oracle(t, rows1, wl.rowwise, wl.columnwise, threads=1)
+        sb1 = W.algorithmic_bytes(rows1, C, True, wl.rowwise, wl.columnwise)
         cpu = {"value": sb / el / 1e9, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": f"rows 0-{rows - 1} of {R} ({100.0 * rows / R:.1f}% of the workload), "
-                         f"all {C} columns, fused, one pass, {el:.2f} s wall"}
+                         f"all {C} columns, fused, one pass, {el:.2f} s wall",
+               "single_thread": {"value": sb1 / el1 / 1e9, "unit": "GB/s", "cores": 1,
+                                 "sample": f"rows 0-{rows1 - 1}, all {C} columns, fused, "
+                                           f"one pass, {el1:.2f} s wall"},
+               "cpu_model": cpu_model(), "arch": platform.machine()}
 
     if rank == 0:
         rec = base_record(args, wl, R, C, world)
@@ -654,6 +690,9 @@ def main():
             "value": value,
             "ms_per_step": ms_per_step,
             "pct_of_peak": 100.0 * achieved / peak,
+            # the same against GB300's nominal HBM3e figure (the benchmark spec's
+            # "~8 TB/s"); the roofline fraction uses the measured copy peak
+            "pct_of_nominal_peak": 100.0 * achieved / NOMINAL_HBM_GBS,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                          "traffic": (profiled_traffic(R, C) if args.workload in (0, 4)

@@ -67,7 +67,7 @@
 extern "C" {
 #endif
 
-#define MXFP8_ABI_VERSION 5
+#define MXFP8_ABI_VERSION 6
 #define MXFP8_BLOCK_SIZE 32
 #define MXFP8_MAX_TENSORS 256
 #define MXFP8_MAX_UPDATE 256
@@ -111,6 +111,13 @@ int rmsnorm_quant_mxfp8(const mxfp8_desc* desc, int n, int rowwise, int columnwi
  * gamma, normed, eps and weight_offset are ignored. Same flags and errors. */
 int quant_mxfp8(const mxfp8_desc* desc, int n, int rowwise, int columnwise,
                 void* stream);
+
+/* The same two calls under the names of the library's first interface
+ * sketch (mxfp8_rmsnorm_quant == rmsnorm_quant_mxfp8, mxfp8_quant ==
+ * quant_mxfp8): identical arguments, behaviour and errors. */
+int mxfp8_rmsnorm_quant(const mxfp8_desc* desc, int n, int rowwise, int columnwise,
+                        void* stream);
+int mxfp8_quant(const mxfp8_desc* desc, int n, int rowwise, int columnwise, void* stream);
 
 /* The same calls with a choice of scale layout (NEXT item of the FSDP page:
  * TE pads its scale planes for compute, `_pad_rowwise_scale`,
@@ -232,6 +239,20 @@ int mm_mxfp8(const void* x, int64_t M, int64_t K, const void* w_q, const void* w
 #define MXFP8_MM_STATIC_SCRATCH_BYTES (32ull << 20)
 int mm_mxfp8_static(const void* x, int64_t M, int64_t K, const void* w_q, const void* w_s,
                     int64_t N, void* out, void* stream);
+
+/* Testing hooks, process-wide, for exercising error paths (the pages have no
+ * counterpart):
+ *   MXFP8_HOOK_FAIL_LAUNCH  value != 0: every later call that passes its
+ *       argument checks returns MXFP8_ERR_CUDA ("invalid argument") as if the
+ *       CUDA runtime had rejected its launch; nothing is launched. 0 restores.
+ *   MXFP8_HOOK_MAX_CLUSTER  value > 0: the fused calls use thread-block
+ *       clusters of at most `value` CTAs (1: one CTA per 32-row stripe, the
+ *       path taken where the device co-schedules no cluster); 0 lifts the cap.
+ * Returns the hook's previous value, or MXFP8_ERR_FLAGS for an unknown hook
+ * or a negative value. Not meant to be set while other threads call. */
+#define MXFP8_HOOK_FAIL_LAUNCH 1
+#define MXFP8_HOOK_MAX_CLUSTER 2
+int mxfp8_set_test_hook(int hook, int value);
 
 /* Text of the last error raised by a call on this host thread ("" if none).
  * The pointer stays valid until the next call on the same thread. */

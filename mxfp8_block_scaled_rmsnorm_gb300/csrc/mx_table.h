@@ -103,4 +103,11 @@ int fused_chunk_cols();
 // for the fused kernel; queried once per device.
 int fused_max_cluster();
 
+// Test hooks (mxfp8_set_test_hook, mxfp8_api.cu). hook_launch_error():
+// cudaErrorInvalidValue while a launch failure is being injected (every
+// launcher returns it before touching the device), else cudaSuccess.
+// hook_max_cluster(): a cap on the fused kernel's cluster size, 0 for none.
+int hook_launch_error();
+int hook_max_cluster();
+
 }  // namespace mx

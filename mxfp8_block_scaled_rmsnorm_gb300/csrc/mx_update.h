@@ -31,5 +31,6 @@ struct UpdTable {
 };
 static_assert(sizeof(UpdTable) < 32000, "kernel parameter limit");
 int launch_update(const UpdTable& t, void* stream);
+int hook_launch_error();  // mxfp8_api.cu: an injected launch error, else cudaSuccess
 
 }  // namespace mx

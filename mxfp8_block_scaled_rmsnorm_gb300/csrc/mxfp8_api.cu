@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -97,7 +98,9 @@ int fill_and_launch(bool fused, const mxfp8_desc* d, const mxfp8_residual* res, 
             const int64_t wide = ceil_div(max_cols, chunk * kWideSlicePasses);
             want = wide > mx::kPortableCluster ? wide : mx::kPortableCluster;
         }
-        const int most = mx::fused_max_cluster();
+        int most = mx::fused_max_cluster();
+        const int cap = mx::hook_max_cluster();
+        if (cap > 0 && cap < most) most = cap;
         cluster = (int)(want < most ? want : most);
         if (cluster < 1) cluster = 1;
     }
@@ -186,6 +189,17 @@ int run(bool fused, const mxfp8_desc* d, const mxfp8_residual* res, int n, int r
 }  // namespace
 
 namespace mx {
+namespace {
+std::atomic<int> g_hook_fail_launch{0};
+std::atomic<int> g_hook_max_cluster{0};
+}  // namespace
+
+int hook_launch_error() {
+    return g_hook_fail_launch.load(std::memory_order_relaxed) ? (int)cudaErrorInvalidValue
+                                                              : (int)cudaSuccess;
+}
+int hook_max_cluster() { return g_hook_max_cluster.load(std::memory_order_relaxed); }
+
 TraceRange::TraceRange(const char* name) { nvtxRangePushA(name); }
 TraceRange::~TraceRange() { nvtxRangePop(); }
 
@@ -315,6 +329,30 @@ int mxfp8_update_planes(const mxfp8_planes* src, const mxfp8_planes* dst, int n,
                     cudaGetErrorString(static_cast<cudaError_t>(err)));
     }
     return MXFP8_OK;
+}
+
+int mxfp8_rmsnorm_quant(const mxfp8_desc* desc, int n, int rowwise, int columnwise,
+                        void* stream) {
+    const mx::TraceRange trace("mxfp8_rmsnorm_quant");
+    return run(true, desc, nullptr, n, rowwise, columnwise, MXFP8_SCALES_COMPACT, stream);
+}
+
+int mxfp8_quant(const mxfp8_desc* desc, int n, int rowwise, int columnwise, void* stream) {
+    const mx::TraceRange trace("mxfp8_quant");
+    return run(false, desc, nullptr, n, rowwise, columnwise, MXFP8_SCALES_COMPACT, stream);
+}
+
+int mxfp8_set_test_hook(int hook, int value) {
+    g_err.clear();
+    if (value < 0) return fail(MXFP8_ERR_FLAGS, "test hook %d: negative value %d", hook, value);
+    switch (hook) {
+        case MXFP8_HOOK_FAIL_LAUNCH:
+            return mx::g_hook_fail_launch.exchange(value != 0 ? 1 : 0);
+        case MXFP8_HOOK_MAX_CLUSTER:
+            return mx::g_hook_max_cluster.exchange(value);
+        default:
+            return fail(MXFP8_ERR_FLAGS, "unknown test hook %d", hook);
+    }
 }
 
 const char* mxfp8_last_error(void) { return g_err.c_str(); }

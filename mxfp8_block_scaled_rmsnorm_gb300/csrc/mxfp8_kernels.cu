@@ -769,6 +769,7 @@ quant_kernel(const __grid_constant__ Table<MAXN> T) {
 template <typename Kern, int MAXN>
 int launch(Kern kern, const Table<MAXN>& t, int64_t grid, int threads, int cluster,
            void* stream, int smem = 0) {
+    if (const int e = hook_launch_error()) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3((unsigned)threads, 1, 1);
@@ -797,6 +798,7 @@ constexpr int kStageBytes = FusedGeo::kRows * FusedGeo::kThreads * 16;
 template <int MAXN, bool MMA, bool RES>
 int launch_staged(const Table<MAXN>& t, int64_t grid, void* stream) {
     auto kern = fused_rmsnorm_quant_kernel<MAXN, MMA, RES>;
+    if (const int e = hook_launch_error()) return e;
     const bool big = t.cluster > kPortableCluster;
     if (t.stage || big) {
         constexpr int kMaxDevices = 64;

@@ -156,6 +156,7 @@ update_planes_kernel(const __grid_constant__ UpdTable T) {
 }  // namespace
 
 int launch_update(const UpdTable& t, void* stream) {
+    if (const int e = hook_launch_error()) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)t.total_chunks, 1, 1);
     cfg.blockDim = dim3(kUpdThreads, 1, 1);

@@ -1,4 +1,12 @@
-"""Parity checks shared by the GPU tests (CUDA path against the CPU oracle)."""
+"""Parity checks shared by the GPU tests (CUDA path against the CPU oracle).
+
+``check_fused`` checks one fused call four ways: (0) its planes equal the
+oracle's quantize of the GPU's own normed output, byte for byte; (1) they equal
+the GPU's standalone quantize of that normed; (2) normed is within one bf16
+step of the oracle's float32 RMSNorm; (3) the GPU's standalone quantize of the
+oracle's normed equals the oracle's planes; (4) the fused planes equal the
+oracle's planes wherever the normed block matches the oracle's.
+"""
 import numpy as np
 import torch
 
@@ -50,6 +58,19 @@ def check_fused(wl, rowwise=True, columnwise=True, threads=None, rows_sample=Non
         R = t.x.shape[0]
         rows = np.arange(R) if rows_sample is None else rows_sample
         x_s = np.ascontiguousarray(t.x[rows])
+        # (0) fused planes == the oracle's quantize of the GPU's own bf16 normed,
+        # byte for byte on every checked row (the Mojo page's description: the
+        # quantize reads the bf16 that lands in outputs_normed). The oracle is a
+        # checker here: its input is the GPU's output, its answer its own.
+        R_q = rows.size - (rows.size % 32 if columnwise else 0)
+        sel_q = rows[:R_q]
+        want = oracle.quant_mxfp8(np.ascontiguousarray(normed[sel_q]), rowwise, columnwise,
+                                  threads=threads)
+        got = (u8(o.q_row)[sel_q] if rowwise else None,
+               u8(o.s_row)[sel_q] if rowwise else None,
+               u8(o.q_col)[sel_q] if columnwise else None,
+               u8(o.s_col)[sel_q.reshape(-1, 32)[:, 0] // 32] if columnwise else None)
+        assert_quant_exact(got, want, "fused planes vs oracle quantize of the GPU normed")
         # (2) normed within 1 bf16 step of the oracle's float32 RMSNorm
         ref = oracle.rmsnorm_f32(x_s, t.gamma, t.eps, t.offset, threads=threads)
         d = ulp_dist_bf16(normed[rows], ref)

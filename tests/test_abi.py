@@ -31,14 +31,14 @@ def test_header_declares_the_calls():
         ["rmsnorm_quant_mxfp8", "quant_mxfp8", "rmsnorm_quant_mxfp8_ex", "quant_mxfp8_ex",
          "add_rmsnorm_quant_mxfp8", "mxfp8_update_planes", "mm_mxfp8",
          "mm_mxfp8_workspace_size", "mm_mxfp8_static", "mxfp8_last_error",
-         "mxfp8_abi_version"])
+         "mxfp8_abi_version", "mxfp8_rmsnorm_quant", "mxfp8_quant", "mxfp8_set_test_hook"])
 
 
 def test_library_exports_every_declared_symbol(mx):
     L = mx.library()
     for name in declared_functions():
         assert hasattr(L, name), name
-    assert L.mxfp8_abi_version() == 5
+    assert L.mxfp8_abi_version() == 6
 
 
 def test_desc_struct_layout_matches_header(mx):
@@ -132,3 +132,74 @@ def test_residual_call_checks_its_pointers(mx):
     res[0].residual, res[0].residual_out = None, 0x20004
     assert L.add_rmsnorm_quant_mxfp8(arr, res, 1, 1, 1, 0, None) == -1
     assert "residual_out" in L.mxfp8_last_error().decode()
+
+
+@pytest.mark.parametrize("fn", ["mxfp8_rmsnorm_quant", "mxfp8_quant"])
+def test_alias_names_check_like_the_main_calls(mx, fn):
+    L = mx.library()
+    getattr(L, fn).argtypes = [ctypes.POINTER(mx.MXFP8Desc), ctypes.c_int, ctypes.c_int,
+                               ctypes.c_int, ctypes.c_void_p]
+    assert getattr(L, fn)(None, 1, 1, 1, None) == -4
+    rc, msg = _call(mx, fn, [_desc(mx, cols=48)])
+    assert rc == -2 and "multiple of 32" in msg
+
+
+HOOK_FAIL_LAUNCH, HOOK_MAX_CLUSTER = 1, 2
+
+
+@pytest.fixture
+def fail_launches(mx):
+    """Every launch reports a CUDA error (injected on the host: nothing reaches
+    a device, so this runs without a GPU)."""
+    L = mx.library()
+    L.mxfp8_set_test_hook.argtypes = [ctypes.c_int, ctypes.c_int]
+    L.mxfp8_set_test_hook.restype = ctypes.c_int
+    prev = L.mxfp8_set_test_hook(HOOK_FAIL_LAUNCH, 1)
+    yield L
+    L.mxfp8_set_test_hook(HOOK_FAIL_LAUNCH, prev)
+
+
+def test_test_hook_arguments(mx):
+    L = mx.library()
+    L.mxfp8_set_test_hook.argtypes = [ctypes.c_int, ctypes.c_int]
+    assert L.mxfp8_set_test_hook(99, 1) == -3
+    assert "unknown test hook" in L.mxfp8_last_error().decode()
+    assert L.mxfp8_set_test_hook(HOOK_MAX_CLUSTER, -1) == -3
+    assert L.mxfp8_set_test_hook(HOOK_MAX_CLUSTER, 4) == 0
+    assert L.mxfp8_set_test_hook(HOOK_MAX_CLUSTER, 0) == 4
+
+
+@pytest.mark.parametrize("fn", ["rmsnorm_quant_mxfp8", "quant_mxfp8", "mxfp8_rmsnorm_quant",
+                                "mxfp8_quant"])
+def test_launch_error_is_reported_as_err_cuda(mx, fail_launches, fn):
+    getattr(fail_launches, fn).argtypes = [ctypes.POINTER(mx.MXFP8Desc), ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    for n in (1, 9):  # the small and the large launch table
+        rc, msg = _call(mx, fn, [_desc(mx, base=0x10000 * (i + 1)) for i in range(n)])
+        assert rc == -5 and msg.startswith("kernel launch failed") and "invalid argument" in msg
+    # argument errors still come first
+    rc, _ = _call(mx, fn, [_desc(mx, cols=48)])
+    assert rc == -2
+
+
+def test_launch_error_in_the_other_calls(mx, fail_launches):
+    L = fail_launches
+    arr = (mx.MXFP8Desc * 1)(_desc(mx))
+    for fn in ("rmsnorm_quant_mxfp8_ex", "quant_mxfp8_ex"):
+        for layout in (0, 1, 2):
+            assert getattr(L, fn)(arr, 1, 1, 1, layout, None) == -5
+            assert "invalid argument" in L.mxfp8_last_error().decode()
+    res = (mx.MXFP8Residual * 1)()
+    res[0].residual, res[0].residual_out = 0x900000, 0xA00000
+    assert L.add_rmsnorm_quant_mxfp8(arr, res, 1, 1, 1, 0, None) == -5
+    src = (mx.MXFP8Planes * 1)()
+    dst = (mx.MXFP8Planes * 1)()
+    for i, o in enumerate((src[0], dst[0])):
+        o.q_row, o.s_row, o.q_col, o.s_col = (0x100000 * (4 * i + k + 1) for k in range(4))
+        o.rows, o.cols = 64, 64
+    assert L.mxfp8_update_planes(src, dst, 1, 1, 1, 2, None) == -5
+    assert "invalid argument" in L.mxfp8_last_error().decode()
+    # the matrix multiply fails at its first launch (the activation quantize)
+    rc = L.mm_mxfp8(0x100000, 256, 256, 0x200000, 0x300000, 256, 0x400000, 0x500000,
+                    1 << 22, None)
+    assert rc == -5 and "invalid argument" in L.mxfp8_last_error().decode()

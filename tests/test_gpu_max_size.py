@@ -1,13 +1,16 @@
 """GPU: one tensor of more than 2^31 elements (65536 x 32800), so element
-offsets past 2^31 exercise the kernels' 64-bit indexing, and 32800 columns
-take the widest cluster (8 CTAs) with several passes per CTA, the last one
-partial (4128 columns per CTA).
+offsets past 2^31 exercise the kernels' 64-bit indexing. 32800 columns take
+the widest cluster the device co-schedules (16 CTAs on GB300, a non-portable
+size): slices of 2080 columns, five 512-column passes per CTA with the last
+one partial, and a last CTA of 1600 columns.
 
 Checked on sampled 32-row stripes (the first, one in the middle and the last
 three, whose offsets lie past 2^31) against the oracle: the quantize planes
-bit-exact, the fused call as in the other fused parity tests (normed within
-one bf16 step; planes equal to a standalone quantize of the GPU's normed on
-the whole tensor, and to the oracle's wherever the normed block matches).
+bit-exact, the fused call as in the other fused parity tests (planes equal to
+the oracle's quantize of the GPU's own normed on the sampled rows; normed
+within one bf16 step; planes equal to a standalone quantize of the GPU's
+normed on the whole tensor, and to the oracle's wherever the normed block
+matches).
 """
 import numpy as np
 import pytest

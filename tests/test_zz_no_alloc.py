@@ -58,12 +58,24 @@ def _bounds(x_bits, w_bits):
 def test_static_matches_workspace_entry_point_twice(lib, M, N, K):
     w_bits = W.random_weights([(N, K)], seed=N + K).tensors[0].x
     wq = mx.quantize_weight_for_mm(to_dev(w_bits))
-    for call, seed in enumerate((M + 1, M + 2)):  # two calls in a row, new operands
-        x_bits = W.random_fused(M, K, seed=seed, scale=2.0).tensors[0].x
-        x = to_dev(x_bits)
-        out_s = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    # two calls in a row on new operands; every tensor is allocated up front, so
+    # that the device's free memory can be compared across the second call
+    xs_bits = [W.random_fused(M, K, seed=M + c, scale=2.0).tensors[0].x for c in (1, 2)]
+    xs = [to_dev(b) for b in xs_bits]
+    outs = [torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+            for _ in xs]
+    torch.cuda.synchronize()
+    free = []
+    for call, (x, out_s) in enumerate(zip(xs, outs)):
+        torch.cuda.empty_cache()
+        free.append(torch.cuda.mem_get_info()[0])
         rc, msg = _static(lib, x, wq, out_s)
         assert rc == 0, msg
+        torch.cuda.synchronize()
+        free.append(torch.cuda.mem_get_info()[0])
+    # the second call (after the first call's set-up) takes no device memory
+    assert free[3] == free[2], f"free device memory changed by {free[2] - free[3]} bytes"
+    for call, (x_bits, x, out_s) in enumerate(zip(xs_bits, xs, outs)):
         out_w = mx.mm_mxfp8(x, wq.q_row, wq.s_row)
         torch.cuda.synchronize()
         ref, bound = _bounds(x_bits, w_bits)
