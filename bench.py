@@ -430,6 +430,9 @@ def run_mm(args, world, rank, local, pg):
         total = sum(a.elapsed_time(b) for a, b in zip(starts, ends))
     else:
         total = starts[0].elapsed_time(ends[-1])
+    status = mx.device_status()
+    if status != 0:
+        raise SystemExit(f"the GEMM reported device status {status:#x}")
     ms = max_over_ranks(total, pg, device) / args.steps
     flops = 2.0 * M * N * K
     tflops = flops / (ms * 1e-3) / 1e12
@@ -445,7 +448,9 @@ def run_mm(args, world, rank, local, pg):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
             "config": {"workload": f"mm_mxfp8-{M}x{N}x{K}", "M": M, "N": N, "K": K,
-                       "gemm": "cuBLASLt 1x32 UE8M0 block-scaled FP8, float32 accumulation",
+                       "gemm": "mxfp8_gemm_kernel: tcgen05 kind::mxf8f6f4 block-scaled "
+                               "(E4M3 x E4M3, UE8M0 per 32), 128x256 tiles, float32 "
+                               "accumulation in tensor memory, bf16 out",
                        "l2": ("operands fit in L2 (%.0f MB): a 256 MB memset and a 256 MB "
                               "read flush L2 before every timed launch, outside its events"
                               % (in_bytes / 1e6)

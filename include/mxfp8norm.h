@@ -201,44 +201,53 @@ int mxfp8_update_planes(const mxfp8_planes* src, const mxfp8_planes* dst, int n,
  *   w_s  its scales in MXFP8_SCALES_MMA_TILED layout (an operand with N rows
  *        and K / 32 scale columns), as quant_mxfp8_ex writes them;
  *   out  bf16 [M, N] row-major.
- * x is quantized rowwise (the encoder of quant_mxfp8) into `workspace`, then
- * cuBLASLt's 1x32 UE8M0 block-scaled FP8 GEMM (float32 accumulation) writes
- * out: two launches on `stream`. cuBLASLt (libcublasLt.so.13) is loaded at the
- * first call. Requirements: K % 32 == 0, N % 16 == 0; every pointer
- * 256-byte aligned; workspace_bytes >= mm_mxfp8_workspace_size(M, K) for the
- * default GEMM workspace (less is accepted down to the quantized activation
- * alone; cuBLASLt then picks among algorithms that fit). The caller owns the
- * workspace; calls that share it must not overlap on the GPU.
- * Errors: MXFP8_ERR_SHAPE, MXFP8_ERR_POINTER, MXFP8_ERR_CUDA (cuBLASLt missing,
- * no algorithm, or a failed launch). */
+ * x is quantized rowwise (the encoder of quant_mxfp8) into `workspace` (codes,
+ * then tiled scales), then this library's block-scaled GEMM on the tensor
+ * cores (tcgen05, E4M3 x E4M3 with UE8M0 block scales, float32 accumulation,
+ * one rounding to bf16) writes out: two launches on `stream`.
+ * Requirements: M, N, K in [1, 2^31), K % 32 == 0, N % 16 == 0; every pointer
+ * 256-byte aligned; workspace_bytes >= mm_mxfp8_workspace_size(M, K). The
+ * caller owns the workspace; calls that share it must not overlap on the GPU.
+ * Errors: MXFP8_ERR_SHAPE, MXFP8_ERR_POINTER, MXFP8_ERR_CUDA (a launch the
+ * runtime rejects, or a TMA tensor map the driver cannot make). */
 size_t mm_mxfp8_workspace_size(int64_t M, int64_t K);
 int mm_mxfp8(const void* x, int64_t M, int64_t K, const void* w_q, const void* w_s, int64_t N,
              void* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* mm_mxfp8 for callers that cannot allocate device memory: the same product,
- * with the scratch it needs (the quantized activation, then cuBLASLt's
- * workspace) taken from a fixed device array inside this library instead of
- * a caller-provided workspace. It is meant for code that must not call
- * cudaMalloc -- e.g. work launched while a CUDA graph is being captured, or a
- * process whose device memory is owned by a caching allocator it cannot reach.
- * The pages have no counterpart of this entry point.
+ * with its scratch (the quantized activation) taken from a fixed device array
+ * inside this library instead of a caller-provided workspace. It is meant for
+ * code that may not call cudaMalloc: a plugin or callback running inside
+ * another framework whose caching allocator owns all device memory and cannot
+ * be reached from here, or a latency-critical loop where cudaMalloc's implicit
+ * device synchronization is not allowed. The pages have no counterpart of this
+ * entry point.
  *
  *  - The array holds MXFP8_MM_STATIC_SCRATCH_BYTES bytes on every GPU that
  *    loads the library, until the process exits. Problems whose quantized
  *    activation, M * K code bytes plus roundup(M, 128) * roundup(K / 32, 4)
  *    scale bytes (each rounded up to 256), does not fit are rejected with
- *    MXFP8_ERR_SHAPE; cuBLASLt gets the rest of the array as its workspace.
+ *    MXFP8_ERR_SHAPE; everything that fits runs.
  *  - The first call on a device does the set-up: it looks up the array's
- *    device address (cudaGetSymbolAddress) and creates this library's
- *    cuBLASLt handle for the device (cuBLASLt reserves a little memory of its
- *    own there). Make that first call before any stream capture. Later calls
- *    call no cudaMalloc, cudaFree or other allocating routine.
- *  - Every call shares the one array and leaves its contents behind; calls
- *    that overlap on the GPU (e.g. on two streams) race and must not be used.
+ *    device address (cudaGetSymbolAddress). Make that first call before any
+ *    stream capture. No call allocates device memory (no cudaMalloc, cudaFree
+ *    or allocating library routine).
+ *  - Every call shares the one array and leaves its contents behind (nothing in
+ *    it needs to start at zero); calls that overlap on the GPU (e.g. on two
+ *    streams) race and must not be used.
  *  - Arguments, layouts and errors as for mm_mxfp8. */
 #define MXFP8_MM_STATIC_SCRATCH_BYTES (32ull << 20)
 int mm_mxfp8_static(const void* x, int64_t M, int64_t K, const void* w_q, const void* w_s,
                     int64_t N, void* out, void* stream);
+
+/* Device-side status of this library's kernels on the current device: 0 if
+ * none has given up since the last clear, else a positive code (bits 48-55:
+ * which wait gave up; bits 0-47: the CTA). The GEMM's waits on its own
+ * pipeline give up after 2 s instead of hanging; the launch then leaves its
+ * output incomplete. Synchronizes the device; clear != 0 resets the status.
+ * Returns MXFP8_ERR_CUDA if the status cannot be read. The pages have no
+ * counterpart. */
+int64_t mxfp8_device_status(int clear);
 
 /* Testing hooks, process-wide, for exercising error paths (the pages have no
  * counterpart):

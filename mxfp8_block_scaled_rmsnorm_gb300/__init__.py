@@ -30,7 +30,7 @@ from typing import Sequence
 import torch
 
 __all__ = ["rmsnorm_quant_mxfp8", "quant_mxfp8", "add_rmsnorm_quant_mxfp8", "update_planes",
-           "mm_mxfp8", "quantize_weight_for_mm",
+           "mm_mxfp8", "quantize_weight_for_mm", "mm_mxfp8_workspace_size", "device_status",
            "NormQuantOut",
            "QuantOut",
            "MXFP8Error", "MXFP8Desc", "library", "make_outputs", "mma_scale_shape",
@@ -116,6 +116,14 @@ def library() -> ctypes.CDLL:
                                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                                ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
         L.mm_mxfp8.restype = ctypes.c_int
+        L.mm_mxfp8_static.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                      ctypes.c_void_p, ctypes.c_void_p]
+        L.mm_mxfp8_static.restype = ctypes.c_int
+        L.mxfp8_device_status.argtypes = [ctypes.c_int]
+        L.mxfp8_device_status.restype = ctypes.c_int64
+        L.mxfp8_set_test_hook.argtypes = [ctypes.c_int, ctypes.c_int]
+        L.mxfp8_set_test_hook.restype = ctypes.c_int
         L.mxfp8_last_error.argtypes = []
         L.mxfp8_last_error.restype = ctypes.c_char_p
         L.mxfp8_abi_version.argtypes = []
@@ -473,4 +481,17 @@ def mm_mxfp8(x: torch.Tensor, w_q: torch.Tensor, w_s: torch.Tensor, out=None,
 
 
 def mm_mxfp8_workspace_size(M: int, K: int) -> int:
+    """Bytes of scratch mm_mxfp8 needs for an [M, K] activation (its
+    quantized codes and tiled scales)."""
     return int(library().mm_mxfp8_workspace_size(M, K))
+
+
+def device_status(clear: bool = True) -> int:
+    """The library's device-side status on the current device (synchronizes):
+    0 when no kernel wait has given up since the last clear, else the code
+    described in include/mxfp8norm.h (mxfp8_device_status)."""
+    L = library()
+    st = int(L.mxfp8_device_status(int(bool(clear))))
+    if st < 0:
+        raise MXFP8Error(st, L.mxfp8_last_error().decode())
+    return st

@@ -19,8 +19,10 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libmxfp8norm.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["mxfp8_kernels.cu", "mxfp8_update.cu", "mxfp8_mm.cu", "mxfp8_api.cu"]
-HEADERS = [os.path.join(CSRC, h) for h in ("mx_table.h", "mx_update.h", "mx_trace.h")] + [
+SOURCES = ["mxfp8_kernels.cu", "mxfp8_update.cu", "mxfp8_gemm.cu", "mxfp8_mm.cu",
+           "mxfp8_api.cu"]
+HEADERS = [os.path.join(CSRC, h) for h in ("mx_table.h", "mx_update.h", "mx_trace.h",
+                                           "mx_gemm.h", "mx_umma.h")] + [
     os.path.join(INCLUDE, "mxfp8norm.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -70,7 +72,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         raise RuntimeError("nvcc failed:\n" + msg)
     if force or procs or _stale(LIB_PATH, objs):
         tmp = LIB_PATH + f".tmp{os.getpid()}"
-        cmd = [nvcc(), *ARCH, "-shared", *objs, "-o", tmp, "-ldl"]
+        cmd = [nvcc(), *ARCH, "-shared", *objs, "-o", tmp]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         subprocess.run(cmd, check=True)

@@ -1,0 +1,508 @@
+// mxfp8_gemm.cu -- block-scaled MXFP8 GEMM on the 5th-generation tensor cores
+// (sm_103a: tcgen05.mma kind::mxf8f6f4 with UE8M0 block scales), the matrix
+// multiply behind mm_mxfp8 (Megatron inference page
+// "core.inference.quantization.utils", `mm_mxfp8`: quantized activation times
+// the quantized weight, float32 accumulation, bf16 output).
+//
+// out[M, N] = sum_k (a[m, k] * 2^(sa[m, k/32] - 127)) * (b[n, k] * 2^(sb[n, k/32] - 127))
+// with a [M, K] and b [N, K] E4M3 codes (K-major: row-major with K contiguous)
+// and sa, sb their scale bytes in the tiled GEMM-operand layout that the
+// quantize kernels write (tiles of 128 rows x 4 scale columns, 512 bytes).
+//
+// Design (one persistent CTA per SM, output tiles of 128 x 256, K in steps of
+// 128 bytes through a 4-stage shared-memory ring):
+//  - warp 0, one thread: producer. Per K step it loads the A tile (128 rows x
+//    128 bytes) and the B tile (256 x 128) with TMA (128-byte swizzle) and the
+//    matching scale tiles (one 512-byte tile for A, two for B: they are
+//    contiguous in the tiled layout) with bulk copies, all completing on the
+//    stage's "full" mbarrier.
+//  - warp 1, one thread: MMA issuer. Per K step it copies the three scale
+//    tiles into tensor memory (tcgen05.cp 32x128b.warpx4) and issues four
+//    128 x 256 x 32 MMAs (scale byte k of each 32-bit scale word for the k-th
+//    32-element block), then commits to the stage's "empty" mbarrier; after the
+//    last K step it commits to "tmem_full".
+//  - warp 2: allocates (and at the end frees) 512 tensor-memory columns: the
+//    float32 accumulator (256 columns) and per-stage scale columns.
+//  - warps 4-11: epilogue. Each reads its 32 accumulator lanes (its TMEM lane
+//    quarter, warp % 4) over 128 columns with tcgen05.ld, converts to bf16
+//    (round to nearest even), releases the accumulator ("tmem_empty"), then
+//    stores, so the next tile's MMAs overlap the stores.
+//  - Every mbarrier wait gives up after a time limit: it records the site in a
+//    device status word (read by mxfp8_device_status), raises a CTA-wide abort
+//    flag that ends the other roles' waits, waits (bounded) for the thread's
+//    own copies and MMAs in flight, and the CTA frees its tensor memory and
+//    exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "mx_gemm.h"
+#include "mx_table.h"
+#include "mx_umma.h"
+
+namespace mx {
+
+__device__ unsigned long long g_gemm_status = 0;
+
+namespace {
+
+constexpr int kBM = 128, kBN = 256, kBK = 128;  // kBK: bytes = E4M3 elements
+constexpr int kStages = 4;
+constexpr int kThreads = 384;
+constexpr int kEpilogueWarp0 = 4;
+constexpr uint32_t kTileA = kBM * kBK;  // 16 KB
+constexpr uint32_t kTileB = kBN * kBK;  // 32 KB
+constexpr uint32_t kSfTile = 512;       // one 128-row x 4 scale tile
+constexpr uint32_t kSfStage = 3 * kSfTile;
+constexpr uint32_t kOffB = kStages * kTileA;
+constexpr uint32_t kOffSf = kOffB + kStages * kTileB;
+constexpr uint32_t kOffBar = kOffSf + kStages * kSfStage;
+constexpr uint32_t kBarBytes = 256;
+constexpr uint32_t kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColSfa = kBN;                     // 4 columns per stage
+constexpr uint32_t kColSfb = kBN + 4 * kStages;       // 8 columns per stage
+static_assert(kColSfb + 8 * kStages <= kTmemCols, "tensor memory budget");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+// Status codes of the sites that can give up (bits 48-55 of the status word;
+// the low bits hold the CTA index).
+enum : uint32_t { kSiteEmpty = 1, kSiteTmemEmpty = 2, kSiteFull = 3, kSiteTmemFull = 4 };
+
+// ------------------------------------------------------------ primitives ---
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void bar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool bar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits until the phase of `bar` with parity `parity` has completed. Gives up
+// after kWaitLimitNs (recording `site` and raising the abort flag), or as soon
+// as another thread of the CTA has given up. Returns whether the phase completed.
+__device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort, uint32_t site) {
+    if (bar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (bar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            *abort = 1u;
+            atomicCAS(&g_gemm_status, 0ull, ((unsigned long long)site << 48) | blockIdx.x);
+            return false;
+        }
+    }
+}
+
+// The same wait, used while draining after an abort: bounded, and not cut
+// short by the abort flag.
+__device__ void drain_bar(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = global_ns();
+    while (!bar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return;
+}
+
+// 2-D TMA load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                            int32_t y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Contiguous bulk copy global -> shared (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Copy one 512-byte scale tile (32 rows x 16 bytes in shared memory) to four
+// tensor-memory columns, replicated into all four 32-lane quarters.
+__device__ __forceinline__ void tc_copy_scales(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+                 : "memory");
+}
+
+// D (+)= A x B with block scales; accumulate selects D += (else D =).
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// 32 consecutive float32 columns of this thread's accumulator lane.
+__device__ __forceinline__ void tc_load32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+        " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31},"
+        " [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tc_wait_load() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t bf16x2(uint32_t lo_f32, uint32_t hi_f32) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(hi_f32)),
+        "f"(__uint_as_float(lo_f32)));
+    return r;
+}
+
+// ----------------------------------------------------------------- kernel ---
+
+__global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    // 128-byte-swizzled tiles must start on 1024-byte boundaries
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+    // bars[0, S): full; [S, 2S): empty; 2S: tmem_full; 2S+1: tmem_empty; 2S+2: drain
+    const uint32_t bar0 = smem_u32(bars);
+    auto full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+    auto empty = [&](int s) { return bar0 + 8u * (uint32_t)(kStages + s); };
+    const uint32_t tmem_full = bar0 + 8u * (2 * kStages);
+    const uint32_t tmem_empty = bar0 + 8u * (2 * kStages + 1);
+    const uint32_t drain = bar0 + 8u * (2 * kStages + 2);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * (2 * kStages + 3));
+    volatile uint32_t* abort = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            bar_init(full(s), 1);
+            bar_init(empty(s), 1);
+        }
+        bar_init(tmem_full, 1);
+        bar_init(tmem_empty, 8);  // one arrival per epilogue warp
+        bar_init(drain, 1);
+        *abort = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------- producer
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t last_par[kStages];
+        bool used[kStages];
+        for (int i = 0; i < kStages; ++i) used[i] = false;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            const int m_blk = tile % p.m_tiles, n_blk = tile / p.m_tiles;
+            const bool second = 2 * n_blk + 1 < p.sfb_row_tiles;
+            const uint32_t tx = kTileA + kTileB + kSfTile * (second ? 3u : 2u);
+            for (int kt = 0; kt < p.k_tiles; ++kt) {
+                if (!wait_bar(empty(s), ph ^ 1u, abort, kSiteEmpty)) {
+                    ok = false;
+                    break;
+                }
+                bar_expect_tx(full(s), tx);
+                tma_load_2d(sbase + s * kTileA, &p.tma_a, kt * kBK, m_blk * kBM, full(s));
+                tma_load_2d(sbase + kOffB + s * kTileB, &p.tma_b, kt * kBK, n_blk * kBN, full(s));
+                const uint32_t sf = sbase + kOffSf + s * kSfStage;
+                bulk_load(sf, p.sfa + ((size_t)m_blk * p.k_tiles + kt) * kSfTile, kSfTile, full(s));
+                bulk_load(sf + kSfTile, p.sfb + ((size_t)(2 * n_blk) * p.k_tiles + kt) * kSfTile,
+                          kSfTile, full(s));
+                if (second)
+                    bulk_load(sf + 2 * kSfTile,
+                              p.sfb + ((size_t)(2 * n_blk + 1) * p.k_tiles + kt) * kSfTile,
+                              kSfTile, full(s));
+                used[s] = true;
+                last_par[s] = ph;
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        if (ok) {
+            // every stage's last release has arrived before the CTA may exit
+            for (int i = 0; i < kStages; ++i) {
+                if (!wait_bar(empty(s), ph ^ 1u, abort, kSiteEmpty)) break;
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        } else {
+            // gave up: the copies already issued land before the CTA exits
+            for (int i = 0; i < kStages; ++i)
+                if (used[i]) drain_bar(full(i), last_par[i]);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------------------------------------------- MMA issuer
+        int s = 0;
+        uint32_t ph = 0, local = 0;
+        bool ok = true;
+        const uint32_t acc = tmem;  // lane 0, column 0
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+            if (!wait_bar(tmem_empty, (local & 1u) ^ 1u, abort, kSiteTmemEmpty)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int kt = 0; kt < p.k_tiles; ++kt) {
+                if (!wait_bar(full(s), ph, abort, kSiteFull)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sf = sbase + kOffSf + s * kSfStage;
+                const uint32_t t_sfa = tmem + kColSfa + 4u * s;
+                const uint32_t t_sfb = tmem + kColSfb + 8u * s;
+                tc_copy_scales(t_sfa, umma::scale_tile_desc(sf));
+                tc_copy_scales(t_sfb, umma::scale_tile_desc(sf + kSfTile));
+                tc_copy_scales(t_sfb + 4u, umma::scale_tile_desc(sf + 2 * kSfTile));
+                const int rem = (p.K - kt * kBK) / 32;
+                const int nk = rem < 4 ? rem : 4;
+                const uint32_t a0 = sbase + s * kTileA;
+                const uint32_t b0 = sbase + kOffB + s * kTileB;
+                for (int k = 0; k < nk; ++k) {
+                    tc_mma(acc, umma::kmajor_sw128_desc(a0 + 32u * k),
+                           umma::kmajor_sw128_desc(b0 + 32u * k),
+                           umma::idesc_mxf8(kBM, kBN, (uint32_t)k, (uint32_t)k), t_sfa, t_sfb,
+                           (kt | k) != 0 ? 1u : 0u);
+                }
+                tc_commit(empty(s));
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            tc_commit(tmem_full);
+        }
+        if (!ok) {
+            // gave up: let this thread's MMAs and scale copies finish first
+            tc_commit(drain);
+            drain_bar(drain, 0);
+        }
+    } else if (warp >= kEpilogueWarp0) {
+        // ---------------------------------------------------- epilogue
+        const int quarter = warp & 3;                       // TMEM lanes 32q .. 32q+31
+        const int half = (warp - kEpilogueWarp0) >> 2;      // accumulator columns 128h ..
+        uint32_t local = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+            const int m_blk = tile % p.m_tiles, n_blk = tile / p.m_tiles;
+            // every lane waits; the warp goes on (converged, as the .sync.aligned
+            // tensor-memory loads need) only if all lanes saw the phase complete
+            const bool ok = wait_bar(tmem_full, local & 1u, abort, kSiteTmemFull);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            tc_fence_after();
+            uint32_t packed[64];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tc_load32(umma::tmem_addr(tmem, 32u * quarter, 128u * half + 32u * c), r);
+                tc_wait_load();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) packed[16 * c + j] = bf16x2(r[2 * j], r[2 * j + 1]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) bar_arrive(tmem_empty);
+            const int64_t row = (int64_t)m_blk * kBM + 32 * quarter + lane;
+            const int64_t col0 = (int64_t)n_blk * kBN + 128 * half;
+            if (row < p.M) {
+                uint16_t* o = p.out + row * p.N + col0;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (col0 + 8 * j < p.N)
+                        *reinterpret_cast<uint4*>(o + 8 * j) =
+                            make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
+                                       packed[4 * j + 3]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------------- host ---
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Tensor map of a K-major E4M3 operand [rows, K]: boxes of 128 bytes of K by
+// box_rows rows, 128-byte swizzle, zero fill outside the matrix.
+int encode_operand(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                   uint32_t box_rows) {
+    EncodeTiled fn = encoder();
+    if (fn == nullptr) return -1;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    const cuuint32_t elem[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : (int)r;
+}
+
+constexpr int kMaxDevices = 64;
+
+}  // namespace
+
+int gemm_prepare(GemmParams* p, const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
+                 const uint8_t* sfb, uint16_t* out, int64_t M, int64_t N, int64_t K) {
+    if (encode_operand(&p->tma_a, a, M, K, kBM) != 0) return -1;
+    if (encode_operand(&p->tma_b, b, N, K, kBN) != 0) return -2;
+    p->sfa = sfa;
+    p->sfb = sfb;
+    p->out = out;
+    p->M = (int32_t)M;
+    p->N = (int32_t)N;
+    p->K = (int32_t)K;
+    p->m_tiles = (int32_t)((M + kBM - 1) / kBM);
+    p->n_tiles = (int32_t)((N + kBN - 1) / kBN);
+    p->k_tiles = (int32_t)((K + kBK - 1) / kBK);
+    p->sfb_row_tiles = (int32_t)((N + 127) / 128);
+    p->num_tiles = p->m_tiles * p->n_tiles;
+    return 0;
+}
+
+int launch_gemm(const GemmParams& p, void* stream) {
+    if (const int e = hook_launch_error()) return e;
+    static int sms[kMaxDevices] = {0};
+    static bool attr[kMaxDevices] = {false};
+    int dev = 0;
+    int err = (int)cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
+    if (!attr[dev]) {
+        err = (int)cudaFuncSetAttribute(mxfp8_gemm_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kSmemBytes);
+        if (err != cudaSuccess) return err;
+        err = (int)cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (err != cudaSuccess) return err;
+        attr[dev] = true;
+    }
+    const int grid = p.num_tiles < sms[dev] ? p.num_tiles : sms[dev];
+    if (grid <= 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cfg.numAttrs = 0;
+    cfg.attrs = nullptr;
+    return (int)cudaLaunchKernelEx(&cfg, mxfp8_gemm_kernel, p);
+}
+
+int gemm_status(bool clear, unsigned long long* out) {
+    // every stream's work first: the copy below is ordered only after the
+    // legacy default stream
+    int err = (int)cudaDeviceSynchronize();
+    if (err != cudaSuccess) return err;
+    err = (int)cudaMemcpyFromSymbol(out, g_gemm_status, sizeof *out);
+    if (err != cudaSuccess) return err;
+    if (clear && *out != 0) {
+        const unsigned long long zero = 0;
+        err = (int)cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof zero);
+    }
+    return err;
+}
+
+}  // namespace mx

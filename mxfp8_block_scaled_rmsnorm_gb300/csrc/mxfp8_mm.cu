@@ -1,29 +1,19 @@
 // mxfp8_mm.cu -- MXFP8 matrix multiply consumer of the planes (Megatron
 // inference page "core.inference.quantization.utils", `mm_mxfp8`: quantize the
-// bf16 activation on the fly, the weight already quantized, then a library
-// block-scaled GEMM; the page dispatches to FlashInfer or scaled_mm).
+// bf16 activation on the fly, the weight already quantized, then a
+// block-scaled GEMM).
 //
 // Here: the activation x [M, K] is quantized rowwise by this library's
-// quantize kernel, with its scales in the tiled GEMM-operand layout, into the
-// caller's workspace; cuBLASLt's 1x32 UE8M0 block-scaled FP8 GEMM (float32
-// accumulation, bf16 output) then computes out = x_q w_q^T. cuBLASLt is
-// column-major, so the product is formed as out^T [N, M] = w_q [N, K] x_q^T,
-// i.e. A = w_q with op T and B = x_q with op N ("TN"), both K-major.
-//
-// cuBLASLt is opened at the first call (dlopen of libcublasLt.so.13), so the
-// library loads and the other entry points work without it.
-#include <cublasLt.h>
+// quantize kernel, with its scales in the tiled GEMM-operand layout, into a
+// scratch area; this library's tcgen05 block-scaled GEMM (mxfp8_gemm.cu) then
+// computes out = x_q w_q^T with float32 accumulation and a bf16 result. Two
+// launches on the caller's stream.
 #include <cuda_runtime.h>
-#include <dlfcn.h>
 
-#include <cstdarg>
-#include <cstdio>
 #include <cstring>
-#include <map>
 #include <mutex>
-#include <string>
-#include <tuple>
 
+#include "mx_gemm.h"
 #include "mx_table.h"
 #include "mx_trace.h"
 #include "mxfp8norm.h"
@@ -34,161 +24,32 @@ int set_error(int code, const char* fmt, ...);  // mxfp8_api.cu
 
 namespace {
 
-struct LtApi {
-    bool ok = false;
-    std::string why;
-    decltype(&cublasLtCreate) create = nullptr;
-    decltype(&cublasLtMatmulDescCreate) desc_create = nullptr;
-    decltype(&cublasLtMatmulDescDestroy) desc_destroy = nullptr;
-    decltype(&cublasLtMatmulDescSetAttribute) desc_set = nullptr;
-    decltype(&cublasLtMatrixLayoutCreate) layout_create = nullptr;
-    decltype(&cublasLtMatrixLayoutDestroy) layout_destroy = nullptr;
-    decltype(&cublasLtMatmulPreferenceCreate) pref_create = nullptr;
-    decltype(&cublasLtMatmulPreferenceDestroy) pref_destroy = nullptr;
-    decltype(&cublasLtMatmulPreferenceSetAttribute) pref_set = nullptr;
-    decltype(&cublasLtMatmulAlgoGetHeuristic) heuristic = nullptr;
-    decltype(&cublasLtMatmul) matmul = nullptr;
-};
-
-LtApi& lt() {
-    static LtApi api;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* h = nullptr;
-        for (const char* name : {"libcublasLt.so.13", "libcublasLt.so"}) {
-            h = dlopen(name, RTLD_NOW | RTLD_GLOBAL);
-            if (h) break;
-        }
-        if (!h) {
-            api.why = std::string("cannot load libcublasLt: ") + dlerror();
-            return;
-        }
-#define MX_SYM(field, sym)                                                   \
-    api.field = reinterpret_cast<decltype(api.field)>(dlsym(h, #sym));       \
-    if (!api.field) {                                                        \
-        api.why = "libcublasLt lacks " #sym;                                 \
-        return;                                                              \
-    }
-        MX_SYM(create, cublasLtCreate)
-        MX_SYM(desc_create, cublasLtMatmulDescCreate)
-        MX_SYM(desc_destroy, cublasLtMatmulDescDestroy)
-        MX_SYM(desc_set, cublasLtMatmulDescSetAttribute)
-        MX_SYM(layout_create, cublasLtMatrixLayoutCreate)
-        MX_SYM(layout_destroy, cublasLtMatrixLayoutDestroy)
-        MX_SYM(pref_create, cublasLtMatmulPreferenceCreate)
-        MX_SYM(pref_destroy, cublasLtMatmulPreferenceDestroy)
-        MX_SYM(pref_set, cublasLtMatmulPreferenceSetAttribute)
-        MX_SYM(heuristic, cublasLtMatmulAlgoGetHeuristic)
-        MX_SYM(matmul, cublasLtMatmul)
-#undef MX_SYM
-        api.ok = true;
-    });
-    return api;
-}
-
-// One cuBLASLt handle per device, and the chosen algorithm per problem.
-struct Plan {
-    cublasLtMatmulDesc_t op = nullptr;
-    cublasLtMatrixLayout_t a = nullptr, b = nullptr, d = nullptr;
-    cublasLtMatmulAlgo_t algo;
-    size_t workspace = 0;
-};
-std::mutex g_mu;
-std::map<int, cublasLtHandle_t> g_handles;
-std::map<std::tuple<int, int64_t, int64_t, int64_t, size_t>, Plan> g_plans;
-
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t align256(int64_t v) { return (v + 255) / 256 * 256; }
 
-// Bytes of the quantized activation inside the workspace: codes, then tiled scales.
+// Bytes of the quantized activation in the scratch: codes, then tiled scales.
 int64_t act_bytes(int64_t M, int64_t K) {
     return align256(M * K) + align256(ceil_div(M, 128) * 128 * ceil_div(K / 32, 4) * 4);
 }
 
-constexpr size_t kGemmWorkspace = size_t(32) << 20;
-
-// Builds (or finds) the plan of an [M, K] x [N, K]^T product; with the mutex held.
-int get_plan(LtApi& api, int dev, cublasLtHandle_t h, int64_t M, int64_t N, int64_t K,
-             size_t ws_limit, const void* a_scale, const void* b_scale, Plan** out) {
-    const auto key = std::make_tuple(dev, M, N, K, ws_limit);
-    auto it = g_plans.find(key);
-    if (it != g_plans.end()) {
-        *out = &it->second;
-        return MXFP8_OK;
-    }
-    Plan p;
-    if (api.desc_create(&p.op, CUBLAS_COMPUTE_32F, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS)
-        return mx::set_error(MXFP8_ERR_CUDA, "cublasLtMatmulDescCreate failed");
-    const cublasOperation_t ta = CUBLAS_OP_T, tb = CUBLAS_OP_N;
-    const cublasLtMatmulMatrixScale_t mode = CUBLASLT_MATMUL_MATRIX_SCALE_VEC32_UE8M0;
-    // the block-scale modes and pointers are set before the heuristic query:
-    // block-scaled algorithms are only offered for a fully described problem
-    bool ok = api.desc_set(p.op, CUBLASLT_MATMUL_DESC_TRANSA, &ta, sizeof ta) == 0 &&
-              api.desc_set(p.op, CUBLASLT_MATMUL_DESC_TRANSB, &tb, sizeof tb) == 0 &&
-              api.desc_set(p.op, CUBLASLT_MATMUL_DESC_A_SCALE_MODE, &mode, sizeof mode) == 0 &&
-              api.desc_set(p.op, CUBLASLT_MATMUL_DESC_B_SCALE_MODE, &mode, sizeof mode) == 0 &&
-              api.desc_set(p.op, CUBLASLT_MATMUL_DESC_A_SCALE_POINTER, &a_scale,
-                           sizeof a_scale) == 0 &&
-              api.desc_set(p.op, CUBLASLT_MATMUL_DESC_B_SCALE_POINTER, &b_scale,
-                           sizeof b_scale) == 0;
-    const int stage_desc = ok;
-    ok = ok && api.layout_create(&p.a, CUDA_R_8F_E4M3, K, N, K) == 0 &&
-         api.layout_create(&p.b, CUDA_R_8F_E4M3, K, M, K) == 0 &&
-         api.layout_create(&p.d, CUDA_R_16BF, N, M, N) == 0;
-    const int stage_layout = ok;
-    cublasLtMatmulPreference_t pref = nullptr;
-    ok = ok && api.pref_create(&pref) == 0 &&
-         api.pref_set(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &ws_limit,
-                      sizeof ws_limit) == 0;
-    const int stage_pref = ok;
-    cublasLtMatmulHeuristicResult_t res;
-    int nres = 0;
-    int hst = -1;
-    if (ok) {
-        hst = (int)api.heuristic(h, p.op, p.a, p.b, p.d, p.d, pref, 1, &res, &nres);
-        ok = hst == 0 && nres > 0;
-    }
-    if (pref) api.pref_destroy(pref);
-    if (!ok) {
-        if (p.a) api.layout_destroy(p.a);
-        if (p.b) api.layout_destroy(p.b);
-        if (p.d) api.layout_destroy(p.d);
-        if (p.op) api.desc_destroy(p.op);
-        return mx::set_error(MXFP8_ERR_CUDA,
-                             "cuBLASLt has no block-scaled FP8 algorithm for M=%lld N=%lld K=%lld "
-                             "(desc %d, layouts %d, preference %d, heuristic status %d, %d results)",
-                             (long long)M, (long long)N, (long long)K, stage_desc, stage_layout,
-                             stage_pref, hst, nres);
-    }
-    p.algo = res.algo;
-    p.workspace = res.workspaceSize;
-    *out = &(g_plans[key] = p);
-    return MXFP8_OK;
-}
-
-// The product with a given scratch area (quantized activation first, then the
-// GEMM's workspace). Pointers and sizes are already checked.
+// The product with a given scratch area (quantized activation: codes, then
+// scales). Pointers and sizes are already checked.
 int mm_run(const void* x, int64_t M, int64_t K, const void* w_q, const void* w_s, int64_t N,
-           void* out, uint8_t* scratch, size_t scratch_bytes, void* stream) {
-    LtApi& api = lt();
-    if (!api.ok) return mx::set_error(MXFP8_ERR_CUDA, "%s", api.why.c_str());
-    const int64_t need_act = act_bytes(M, K);
-
+           void* out, uint8_t* scratch, void* stream) {
     // 1. quantize x rowwise into the scratch, scales tiled for the GEMM. The
-    // tiled scale buffer has padding rows / columns when M % 128 or
-    // (K / 32) % 4 is not zero; the GEMM may read them, so they are zeroed
-    // (byte 0 is the scale 2^-127; leftover bytes could be 0xFF, a NaN scale).
+    // tiled buffer's padding (rows past M, scale columns past K / 32) is never
+    // read: the GEMM's rows past M are not stored and its last K step issues
+    // only the 32-column blocks that exist.
     uint8_t* xq = scratch;
     uint8_t* xs = xq + align256(M * K);
-    if (M % 128 != 0 || (K / 32) % 4 != 0) {
-        const cudaError_t e = cudaMemsetAsync(xs, 0, (size_t)(need_act - align256(M * K)),
-                                              static_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            return mx::set_error(MXFP8_ERR_CUDA, "clearing the scale padding failed: %s",
-                                 cudaGetErrorString(e));
-        }
-    }
+    mx::GemmParams gp;
+    std::memset(&gp, 0, sizeof gp);
+    const int mr = mx::gemm_prepare(&gp, xq, xs, static_cast<const uint8_t*>(w_q),
+                                    static_cast<const uint8_t*>(w_s),
+                                    static_cast<uint16_t*>(out), M, N, K);
+    if (mr != 0)
+        return mx::set_error(MXFP8_ERR_CUDA, "cannot make the TMA tensor map of %s",
+                             mr == -1 ? "x" : "w_q");
     mx::Table<mx::kSmallTable> t;
     std::memset(&t, 0, sizeof t);
     t.n = 1;
@@ -208,46 +69,25 @@ int mm_run(const void* x, int64_t M, int64_t K, const void* w_q, const void* w_s
         return mx::set_error(MXFP8_ERR_CUDA, "quantize launch failed: %s",
                              cudaGetErrorString(static_cast<cudaError_t>(err)));
     }
-
-    // 2. out^T = w_q x_q^T on cuBLASLt
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    // 2. out = x_q w_q^T on the tensor cores
+    err = mx::launch_gemm(gp, stream);
+    if (err != cudaSuccess) {
         cudaGetLastError();
-        return mx::set_error(MXFP8_ERR_CUDA, "cudaGetDevice failed");
+        return mx::set_error(MXFP8_ERR_CUDA, "GEMM launch failed: %s",
+                             cudaGetErrorString(static_cast<cudaError_t>(err)));
     }
-    uint8_t* gemm_ws = xq + need_act;
-    const size_t gemm_ws_bytes = scratch_bytes - (size_t)need_act;
-    std::lock_guard<std::mutex> lock(g_mu);
-    cublasLtHandle_t& h = g_handles[dev];
-    if (h == nullptr && api.create(&h) != CUBLAS_STATUS_SUCCESS) {
-        h = nullptr;
-        return mx::set_error(MXFP8_ERR_CUDA, "cublasLtCreate failed");
-    }
-    Plan* p = nullptr;
-    const void* a_scale = w_s;
-    const void* b_scale = xs;
-    const int rc = get_plan(api, dev, h, M, N, K, gemm_ws_bytes, a_scale, b_scale, &p);
-    if (rc != MXFP8_OK) return rc;
-    if (api.desc_set(p->op, CUBLASLT_MATMUL_DESC_A_SCALE_POINTER, &a_scale, sizeof a_scale) ||
-        api.desc_set(p->op, CUBLASLT_MATMUL_DESC_B_SCALE_POINTER, &b_scale, sizeof b_scale))
-        return mx::set_error(MXFP8_ERR_CUDA, "cannot set the scale pointers");
-    const float alpha = 1.0f, beta = 0.0f;
-    const cublasStatus_t st = api.matmul(h, p->op, &alpha, w_q, p->a, xq, p->b, &beta, out, p->d,
-                                         out, p->d, &p->algo, gemm_ws, gemm_ws_bytes,
-                                         static_cast<cudaStream_t>(stream));
-    if (st != CUBLAS_STATUS_SUCCESS)
-        return mx::set_error(MXFP8_ERR_CUDA, "cublasLtMatmul failed with status %d", (int)st);
     return MXFP8_OK;
 }
 
 int check_mm_args(const void* x, int64_t M, int64_t K, const void* w_q, const void* w_s,
                   int64_t N, void* out) {
-    if (M <= 0 || N <= 0 || K <= 0 || K % 32 != 0 || N % 16 != 0 || M > (int64_t(1) << 31) ||
-        N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+    constexpr int64_t kMax = (int64_t(1) << 31) - 1;
+    if (M <= 0 || N <= 0 || K <= 0 || K % 32 != 0 || N % 16 != 0 || M > kMax || N > kMax ||
+        K > kMax || ceil_div(M, 128) * ceil_div(N, 256) > kMax)
         return mx::set_error(MXFP8_ERR_SHAPE,
-                             "mm_mxfp8 needs M, N, K > 0, K %% 32 == 0 and N %% 16 == 0 "
-                             "(got M=%lld N=%lld K=%lld)", (long long)M, (long long)N,
-                             (long long)K);
+                             "mm_mxfp8 needs M, N, K in [1, 2^31), K %% 32 == 0 and "
+                             "N %% 16 == 0 (got M=%lld N=%lld K=%lld)", (long long)M,
+                             (long long)N, (long long)K);
     const void* ptrs[] = {x, w_q, w_s, out};
     const char* names[] = {"x", "w_q", "w_s", "out"};
     for (int i = 0; i < 4; ++i)
@@ -265,6 +105,7 @@ int check_mm_args(const void* x, int64_t M, int64_t K, const void* w_q, const vo
 static __device__ __align__(256) uint8_t g_mm_static_scratch[MXFP8_MM_STATIC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
 uint8_t* g_static_ptr[kMaxDevices] = {nullptr};
 
 // Device address of the static scratch on the current device (set-up on the
@@ -275,7 +116,7 @@ int static_scratch(uint8_t** out) {
         cudaGetLastError();
         return mx::set_error(MXFP8_ERR_CUDA, "no usable current device");
     }
-    std::lock_guard<std::mutex> lock(g_mu);
+    std::lock_guard<std::mutex> lock(g_static_mu);
     if (g_static_ptr[dev] == nullptr) {
         void* p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_mm_static_scratch);
@@ -296,7 +137,7 @@ extern "C" {
 
 size_t mm_mxfp8_workspace_size(int64_t M, int64_t K) {
     if (M <= 0 || K <= 0 || K % 32 != 0) return 0;
-    return (size_t)act_bytes(M, K) + kGemmWorkspace;
+    return (size_t)act_bytes(M, K);
 }
 
 int mm_mxfp8(const void* x, int64_t M, int64_t K, const void* w_q, const void* w_s, int64_t N,
@@ -311,8 +152,7 @@ int mm_mxfp8(const void* x, int64_t M, int64_t K, const void* w_q, const void* w
     if ((int64_t)workspace_bytes < need_act)
         return mx::set_error(MXFP8_ERR_SHAPE, "workspace of %zu bytes < %lld needed",
                              workspace_bytes, (long long)need_act);
-    return mm_run(x, M, K, w_q, w_s, N, out, static_cast<uint8_t*>(workspace), workspace_bytes,
-                  stream);
+    return mm_run(x, M, K, w_q, w_s, N, out, static_cast<uint8_t*>(workspace), stream);
 }
 
 int mm_mxfp8_static(const void* x, int64_t M, int64_t K, const void* w_q, const void* w_s,
@@ -331,8 +171,19 @@ int mm_mxfp8_static(const void* x, int64_t M, int64_t K, const void* w_q, const 
     uint8_t* scratch = nullptr;
     rc = static_scratch(&scratch);
     if (rc != MXFP8_OK) return rc;
-    return mm_run(x, M, K, w_q, w_s, N, out, scratch, (size_t)MXFP8_MM_STATIC_SCRATCH_BYTES,
-                  stream);
+    return mm_run(x, M, K, w_q, w_s, N, out, scratch, stream);
+}
+
+int64_t mxfp8_device_status(int clear) {
+    mx::set_error(MXFP8_OK, "");
+    unsigned long long st = 0;
+    const int err = mx::gemm_status(clear != 0, &st);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return mx::set_error(MXFP8_ERR_CUDA, "cannot read the device status: %s",
+                             cudaGetErrorString(static_cast<cudaError_t>(err)));
+    }
+    return (int64_t)st;
 }
 
 }  // extern "C"
