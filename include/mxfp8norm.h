@@ -241,11 +241,17 @@ int mm_mxfp8_static(const void* x, int64_t M, int64_t K, const void* w_q, const 
                     int64_t N, void* out, void* stream);
 
 /* Device-side status of this library's kernels on the current device: 0 if
- * none has given up since the last clear, else a positive code (bits 48-55:
- * which wait gave up; bits 0-47: the CTA). The GEMM's waits on its own
- * pipeline give up after 2 s instead of hanging; the launch then leaves its
- * output incomplete. Synchronizes the device; clear != 0 resets the status.
- * Returns MXFP8_ERR_CUDA if the status cannot be read. The pages have no
+ * nothing was recorded since the last clear, else a positive code:
+ *  - bits 48-55 in 1..4: a wait of the GEMM on its own pipeline gave up after
+ *    2 s instead of hanging (bits 0-47: the CTA); that launch left its output
+ *    incomplete;
+ *  - bits 48-55 in 0x81..0x89 (bounds-checking build libmxfp8norm_bounds.so
+ *    only): a quantize kernel computed an access outside the extent this
+ *    header states for a buffer, and skipped it (bits 0-47: the element
+ *    offset; 0x81 x, 0x82 residual, 0x83 residual_out, 0x84 gamma,
+ *    0x85 normed, 0x86 q_row, 0x87 s_row, 0x88 q_col, 0x89 s_col).
+ * Synchronizes the device; clear != 0 resets the status. Returns
+ * MXFP8_ERR_CUDA if the status cannot be read. The pages have no
  * counterpart. */
 int64_t mxfp8_device_status(int clear);
 

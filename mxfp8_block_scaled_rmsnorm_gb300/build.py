@@ -18,6 +18,11 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libmxfp8norm.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
+# The bounds-checking build: the same library with the quantize kernels
+# compiled with -DMXFP8_DEBUG_BOUNDS (every global access checked against the
+# extents the C ABI states; violations recorded in mxfp8_device_status).
+BOUNDS_LIB_PATH = os.path.join(PKG, "libmxfp8norm_bounds.so")
+BOUNDS_SOURCE = "mxfp8_kernels.cu"
 
 SOURCES = ["mxfp8_kernels.cu", "mxfp8_update.cu", "mxfp8_gemm.cu", "mxfp8_mm.cu",
            "mxfp8_api.cu"]
@@ -45,15 +50,19 @@ def _stale(target: str, deps) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile and link the library if any source or header is newer; return its path."""
+    """Compile and link the library (and its bounds-checking twin) if any source
+    or header is newer; return the library's path."""
     os.makedirs(BUILD_DIR, exist_ok=True)
     objs, procs = [], []
-    for src in SOURCES:
+    jobs = [(src, os.path.join(BUILD_DIR, src.replace(".cu", ".o")), []) for src in SOURCES]
+    bounds_obj = os.path.join(BUILD_DIR, BOUNDS_SOURCE.replace(".cu", "_bounds.o"))
+    jobs.append((BOUNDS_SOURCE, bounds_obj, ["-DMXFP8_DEBUG_BOUNDS"]))
+    for src, obj, extra in jobs:
         path = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        objs.append(obj)
+        if not extra:
+            objs.append(obj)
         if force or _stale(obj, [path, *HEADERS]):
-            cmd = [nvcc(), *NVCC_FLAGS, "-c", path, "-o", obj]
+            cmd = [nvcc(), *NVCC_FLAGS, *extra, "-c", path, "-o", obj]
             if ptxas_info:
                 cmd.insert(1, "-Xptxas=-v")
             if verbose:
@@ -70,13 +79,16 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if failed:
         msg = "\n".join(" ".join(c) + "\n" + o for c, o in failed)
         raise RuntimeError("nvcc failed:\n" + msg)
-    if force or procs or _stale(LIB_PATH, objs):
-        tmp = LIB_PATH + f".tmp{os.getpid()}"
-        cmd = [nvcc(), *ARCH, "-shared", *objs, "-o", tmp]
-        if verbose:
-            print(" ".join(cmd), file=sys.stderr)
-        subprocess.run(cmd, check=True)
-        os.replace(tmp, LIB_PATH)
+    kernels_obj = os.path.join(BUILD_DIR, BOUNDS_SOURCE.replace(".cu", ".o"))
+    bounds_objs = [bounds_obj if o == kernels_obj else o for o in objs]
+    for lib, lib_objs in ((LIB_PATH, objs), (BOUNDS_LIB_PATH, bounds_objs)):
+        if force or procs or _stale(lib, lib_objs):
+            tmp = lib + f".tmp{os.getpid()}"
+            cmd = [nvcc(), *ARCH, "-shared", *lib_objs, "-o", tmp]
+            if verbose:
+                print(" ".join(cmd), file=sys.stderr)
+            subprocess.run(cmd, check=True)
+            os.replace(tmp, lib)
     return LIB_PATH
 
 

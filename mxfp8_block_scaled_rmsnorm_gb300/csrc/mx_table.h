@@ -103,6 +103,10 @@ int fused_chunk_cols();
 // for the fused kernel; queried once per device.
 int fused_max_cluster();
 
+// Status word of the bounds-checking build (always 0 in the normal build),
+// read with a synchronizing copy; cleared when asked.
+int bounds_status(bool clear, unsigned long long* out);
+
 // Test hooks (mxfp8_set_test_hook, mxfp8_api.cu). hook_launch_error():
 // cudaErrorInvalidValue while a launch failure is being injected (every
 // launcher returns it before touching the device), else cudaSuccess.

@@ -61,7 +61,36 @@
 #include "mx_table.h"
 
 namespace mx {
+
+// Bounds-checking build (-DMXFP8_DEBUG_BOUNDS): every global access of the two
+// kernels is checked against the extent of its buffer that the C ABI states
+// for the entry's shape and scale layout; an access outside it is skipped and
+// the first one is recorded in g_bounds_status (bits 48-55: 0x80 | the access
+// site; bits 0-47: the element offset), which mxfp8_device_status reports.
+// In the normal build the checks compile to nothing.
+#ifdef MXFP8_DEBUG_BOUNDS
+__device__ unsigned long long g_bounds_status = 0;
+#endif
+
 namespace {
+
+enum BoundsSite : uint32_t {
+    kSiteX = 1, kSiteResIn, kSiteResOut, kSiteGamma, kSiteNormed,
+    kSiteQRow, kSiteSRow, kSiteQCol, kSiteSCol
+};
+
+#ifdef MXFP8_DEBUG_BOUNDS
+__device__ __noinline__ bool in_bounds(int64_t off, int64_t len, int64_t extent, uint32_t site) {
+    if (off >= 0 && off + len <= extent) return true;
+    atomicCAS(&g_bounds_status, 0ull,
+              ((unsigned long long)(0x80u | site) << 48) |
+                  ((unsigned long long)off & 0xFFFFFFFFFFFFull));
+    return false;
+}
+#define MX_IN(off, len, extent, site) in_bounds((off), (len), (extent), (site))
+#else
+#define MX_IN(off, len, extent, site) true
+#endif
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -205,6 +234,17 @@ struct TileAt {
 
 __device__ __forceinline__ int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
+// Extents (in bytes) of the scale buffers of the entry `at` belongs to, as the
+// C ABI states them for each layout.
+__device__ __forceinline__ int64_t srow_extent(const TileAt& at) {
+    const int64_t nb = at.cols / kBlock;
+    return (at.mma || at.padded) ? round_up(at.rows, 128) * round_up(nb, 4) : at.rows * nb;
+}
+__device__ __forceinline__ int64_t scol_extent(const TileAt& at) {
+    const int64_t sb = at.rows / kBlock;
+    return (at.mma || at.padded) ? round_up(sb, 4) * round_up(at.cols, 128) : sb * at.cols;
+}
+
 // Byte offset of scale (m, k) in the tiled GEMM-operand layout: tiles of 128
 // rows x 4 scale columns, 512 bytes each, row tiles outer; inside a tile, row
 // m and column k sit at (m % 32) * 16 + ((m / 32) % 4) * 4 + k % 4.
@@ -238,12 +278,16 @@ __device__ __forceinline__ void store_col_scales(uint8_t* s_col, const TileAt& a
                                                  uint32_t hi4) {
     if (!at.mma) {
         const int64_t cp = at.padded ? round_up(at.cols, 128) : at.cols;
-        *reinterpret_cast<uint2*>(s_col + at.stripe * cp + at.col) = make_uint2(lo4, hi4);
+        if (MX_IN(at.stripe * cp + at.col, 8, scol_extent(at), kSiteSCol))
+            *reinterpret_cast<uint2*>(s_col + at.stripe * cp + at.col) = make_uint2(lo4, hi4);
         return;
     }
-    uint8_t* sc = s_col + mma_off(at.col, at.stripe, ((at.rows >> 5) + 3) >> 2);
+    const int64_t o = mma_off(at.col, at.stripe, ((at.rows >> 5) + 3) >> 2);
+    uint8_t* sc = s_col + o;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) sc[16 * j] = (uint8_t)(((j < 4 ? lo4 : hi4) >> (8 * (j & 3))) & 0xFFu);
+    for (int j = 0; j < 8; ++j)
+        if (MX_IN(o + 16 * j, 1, scol_extent(at), kSiteSCol))
+            sc[16 * j] = (uint8_t)(((j < 4 ? lo4 : hi4) >> (8 * (j & 3))) & 0xFFu);
 }
 
 // Both planes of a thread tile y[] whose maxima were folded into m, with bf16
@@ -280,14 +324,20 @@ __device__ __forceinline__ void quantize_tile(const uint4 (&y)[G::kRows], TileMa
             const uint32_t s_odd = __byte_perm(sc2, 0, 0x3232);   // row 2j+1
             if (at.col_ok) {
                 if (2 * j < at.nrows) {
-                    __stcs(reinterpret_cast<uint2*>(qr + (2 * j) * at.cols),
-                           quant8(y[2 * j], s_even, s_even, s_even, s_even));
-                    if (writes_scale) sr[(2 * j) * rp] = (uint8_t)(bytes2 & 0xFFu);
+                    if (MX_IN(base + (2 * j) * at.cols, 8, at.rows * at.cols, kSiteQRow))
+                        __stcs(reinterpret_cast<uint2*>(qr + (2 * j) * at.cols),
+                               quant8(y[2 * j], s_even, s_even, s_even, s_even));
+                    if (writes_scale &&
+                        MX_IN((sr - s_row) + (2 * j) * rp, 1, srow_extent(at), kSiteSRow))
+                        sr[(2 * j) * rp] = (uint8_t)(bytes2 & 0xFFu);
                 }
                 if (2 * j + 1 < at.nrows) {
-                    __stcs(reinterpret_cast<uint2*>(qr + (2 * j + 1) * at.cols),
-                           quant8(y[2 * j + 1], s_odd, s_odd, s_odd, s_odd));
-                    if (writes_scale) sr[(2 * j + 1) * rp] = (uint8_t)(bytes2 >> 16);
+                    if (MX_IN(base + (2 * j + 1) * at.cols, 8, at.rows * at.cols, kSiteQRow))
+                        __stcs(reinterpret_cast<uint2*>(qr + (2 * j + 1) * at.cols),
+                               quant8(y[2 * j + 1], s_odd, s_odd, s_odd, s_odd));
+                    if (writes_scale &&
+                        MX_IN((sr - s_row) + (2 * j + 1) * rp, 1, srow_extent(at), kSiteSRow))
+                        sr[(2 * j + 1) * rp] = (uint8_t)(bytes2 >> 16);
                 }
             }
         }
@@ -311,7 +361,7 @@ __device__ __forceinline__ void quantize_tile(const uint4 (&y)[G::kRows], TileMa
             uint8_t* qc = q_col + base;
 #pragma unroll
             for (int i = 0; i < G::kRows; ++i)
-                if (i < at.nrows)
+                if (i < at.nrows && MX_IN(base + i * at.cols, 8, at.rows * at.cols, kSiteQCol))
                     __stcs(reinterpret_cast<uint2*>(qc + i * at.cols),
                            quant8(y[i], sc[0], sc[1], sc[2], sc[3]));
         }
@@ -382,12 +432,14 @@ __device__ __forceinline__ void emit_planes(const uint4 (&y)[G::kRows], TileMax<
             const uint32_t byte = (i & 1) ? (rbytes[i >> 1] >> 16) : (rbytes[i >> 1] & 0xFFu);
             const float s = inv_scale(byte);
             const uint64_t ss = pair(s, s);
-            st_code8(reinterpret_cast<uint2*>(q_row + base + i * C),
-                   make_uint2(e4m3x4(mul2(p0, ss), mul2(p1, ss)),
-                              e4m3x4(mul2(p2, ss), mul2(p3, ss))), lines);
-            if (writes_row_scale) sr[i * rp] = (uint8_t)byte;
+            if (MX_IN(base + i * C, 8, at.rows * C, kSiteQRow))
+                st_code8(reinterpret_cast<uint2*>(q_row + base + i * C),
+                       make_uint2(e4m3x4(mul2(p0, ss), mul2(p1, ss)),
+                                  e4m3x4(mul2(p2, ss), mul2(p3, ss))), lines);
+            if (writes_row_scale && MX_IN((sr - s_row) + i * rp, 1, srow_extent(at), kSiteSRow))
+                sr[i * rp] = (uint8_t)byte;
         }
-        if (do_col)
+        if (do_col && MX_IN(base + i * C, 8, at.rows * C, kSiteQCol))
             st_code8(reinterpret_cast<uint2*>(q_col + base + i * C),
                    make_uint2(e4m3x4(mul2(p0, cscale[0]), mul2(p1, cscale[1])),
                               e4m3x4(mul2(p2, cscale[2]), mul2(p3, cscale[3]))), lines);
@@ -473,10 +525,10 @@ __device__ __forceinline__ uint4 ld_x(const uint16_t* p, bool keep_in_l2) {
 // otherwise stream it (ld.global.cs, evict first).
 template <int kR, bool FULL, bool KEEP>
 __device__ __forceinline__ void load_tile(uint4 (&xv)[kR], const uint16_t* p, int64_t C,
-                                          bool col_ok, int nrows) {
+                                          bool col_ok, int nrows, int64_t off, int64_t extent) {
 #pragma unroll
     for (int i = 0; i < kR; ++i) {
-        if (FULL || (col_ok && i < nrows)) {
+        if ((FULL || (col_ok && i < nrows)) && MX_IN(off + i * C, 8, extent, kSiteX)) {
             const uint4* a = reinterpret_cast<const uint4*>(p + i * C);
             xv[i] = KEEP ? __ldcg(a) : __ldcs(a);
         } else {
@@ -518,7 +570,7 @@ __device__ __forceinline__ void add_residual_tile(uint4 (&xv)[kR], const DevDesc
     if (D.res_in != nullptr) {
 #pragma unroll
         for (int i = 0; i < kR; ++i) {
-            if (ok && i < nrows) {
+            if (ok && i < nrows && MX_IN(base + i * C, 8, D.rows * C, kSiteResIn)) {
                 const uint4* a = reinterpret_cast<const uint4*>(D.res_in + base + i * C);
                 const uint4 r = keep ? __ldcg(a) : __ldcs(a);
                 xv[i].x = add_bf16x2(xv[i].x, r.x);
@@ -531,7 +583,8 @@ __device__ __forceinline__ void add_residual_tile(uint4 (&xv)[kR], const DevDesc
     if (write_out && D.res_out != nullptr) {
 #pragma unroll
         for (int i = 0; i < kR; ++i)
-            if (ok && i < nrows) *reinterpret_cast<uint4*>(D.res_out + base + i * C) = xv[i];
+            if (ok && i < nrows && MX_IN(base + i * C, 8, D.rows * C, kSiteResOut))
+                *reinterpret_cast<uint4*>(D.res_out + base + i * C) = xv[i];
     }
 }
 
@@ -598,16 +651,21 @@ fused_rmsnorm_quant_kernel(const __grid_constant__ Table<MAXN> T) {
         if (staged) {
 #pragma unroll
             for (int i = 0; i < kR; ++i)
-                if (ok && i < at.nrows)
+                if (ok && i < at.nrows &&
+                    MX_IN(at.row0 * C + c + i * C, 8, R * C, kSiteResIn))
                     cp_async16(&rstage[i * G::kThreads + tid], D.res_in + at.row0 * C + c + i * C);
         }
         if (warp_full(ok && at.nrows == kR)) {
 #pragma unroll
-            for (int i = 0; i < kR; ++i) xv[i] = ld_x(p + i * C, keep_x);
+            for (int i = 0; i < kR; ++i)
+                xv[i] = MX_IN(at.row0 * C + c + i * C, 8, R * C, kSiteX) ? ld_x(p + i * C, keep_x)
+                                                                          : make_uint4(0, 0, 0, 0);
         } else {
 #pragma unroll
             for (int i = 0; i < kR; ++i)
-                xv[i] = (ok && i < at.nrows) ? ld_x(p + i * C, keep_x) : make_uint4(0, 0, 0, 0);
+                xv[i] = (ok && i < at.nrows && MX_IN(at.row0 * C + c + i * C, 8, R * C, kSiteX))
+                            ? ld_x(p + i * C, keep_x)
+                            : make_uint4(0, 0, 0, 0);
         }
         // h = x + residual, written out here; the residual is kept in L2 for
         // the pass-2 re-read only when h is not written (else h is re-read)
@@ -616,12 +674,15 @@ fused_rmsnorm_quant_kernel(const __grid_constant__ Table<MAXN> T) {
 #pragma unroll
             for (int i = 0; i < kR; ++i) {
                 if (ok && i < at.nrows) {
+                    // (the staged copy was skipped, and this slot is stale, only
+                    // where the bounds-checking build reports an access)
                     const uint4 r = rstage[i * G::kThreads + tid];
                     xv[i].x = add_bf16x2(xv[i].x, r.x);
                     xv[i].y = add_bf16x2(xv[i].y, r.y);
                     xv[i].z = add_bf16x2(xv[i].z, r.z);
                     xv[i].w = add_bf16x2(xv[i].w, r.w);
-                    if (D.res_out != nullptr)
+                    if (D.res_out != nullptr &&
+                        MX_IN(at.row0 * C + c + i * C, 8, R * C, kSiteResOut))
                         *reinterpret_cast<uint4*>(D.res_out + at.row0 * C + c + i * C) = xv[i];
                 }
             }
@@ -672,13 +733,15 @@ fused_rmsnorm_quant_kernel(const __grid_constant__ Table<MAXN> T) {
             const uint16_t* src = (RES && D.res_out != nullptr) ? D.res_out : D.x;
 #pragma unroll
             for (int i = 0; i < kR; ++i)
-                xv[i] = (at.col_ok && i < at.nrows) ? ld_x(src + base + i * C, false)
-                                                    : make_uint4(0, 0, 0, 0);
+                xv[i] = (at.col_ok && i < at.nrows &&
+                         MX_IN(base + i * C, 8, R * C, src == D.x ? kSiteX : kSiteResOut))
+                            ? ld_x(src + base + i * C, false)
+                            : make_uint4(0, 0, 0, 0);
             if (RES && D.res_out == nullptr)
                 add_residual_tile<kR>(xv, D, base, C, at.col_ok, at.nrows, false, false);
         }
         uint64_t ww[4];
-        if (at.col_ok) {
+        if (at.col_ok && MX_IN(at.col, 8, C, kSiteGamma)) {
             const uint4 gv = __ldg(reinterpret_cast<const uint4*>(D.gamma + at.col));
             const float o = D.offset;
             ww[0] = pair(bf16lo(gv.x) + o, bf16hi(gv.x) + o);
@@ -703,7 +766,8 @@ fused_rmsnorm_quant_kernel(const __grid_constant__ Table<MAXN> T) {
             y.w = norm2(xi.w, rr, ww[3]);
             xv[i] = y;
             // streaming store, as for the codes (never read by this kernel)
-            if (at.col_ok && i < at.nrows) __stcs(reinterpret_cast<uint4*>(nrm + i * C), y);
+            if (at.col_ok && i < at.nrows && MX_IN(base + i * C, 8, R * C, kSiteNormed))
+                __stcs(reinterpret_cast<uint4*>(nrm + i * C), y);
             fold_col(m, y);
             if (i & 1) fold_rows(m, i >> 1, xv[i - 1], y);
         }
@@ -748,7 +812,8 @@ quant_kernel(const __grid_constant__ Table<MAXN> T) {
     TileMax<G> m;
     m.colmax[0] = m.colmax[1] = m.colmax[2] = m.colmax[3] = 0u;
     if (warp_full(at.col_ok && at.nrows == kR)) {
-        load_tile<kR, true, false>(xv, p, at.cols, at.col_ok, at.nrows);
+        load_tile<kR, true, false>(xv, p, at.cols, at.col_ok, at.nrows,
+                                   at.row0 * at.cols + at.col, at.rows * at.cols);
 #pragma unroll
         for (int i = 0; i < kR; ++i) {
             fold_col(m, xv[i]);
@@ -756,7 +821,8 @@ quant_kernel(const __grid_constant__ Table<MAXN> T) {
         }
         emit_planes<G, true>(xv, m, at, D.q_row, D.s_row, D.q_col, D.s_col, do_row, do_col, g, q);
     } else {
-        load_tile<kR, false, false>(xv, p, at.cols, at.col_ok, at.nrows);
+        load_tile<kR, false, false>(xv, p, at.cols, at.col_ok, at.nrows,
+                                    at.row0 * at.cols + at.col, at.rows * at.cols);
 #pragma unroll
         for (int i = 0; i < kR; ++i) {
             fold_col(m, xv[i]);
@@ -853,6 +919,24 @@ int launch_quant(const Table<kLargeTable>& t, int64_t grid, void* stream) {
 }
 
 int fused_chunk_cols() { return FusedGeo::kChunk; }
+
+int bounds_status(bool clear, unsigned long long* out) {
+    *out = 0;
+#ifdef MXFP8_DEBUG_BOUNDS
+    int err = (int)cudaDeviceSynchronize();
+    if (err != cudaSuccess) return err;
+    err = (int)cudaMemcpyFromSymbol(out, g_bounds_status, sizeof *out);
+    if (err != cudaSuccess) return err;
+    if (clear && *out != 0) {
+        const unsigned long long zero = 0;
+        err = (int)cudaMemcpyToSymbol(g_bounds_status, &zero, sizeof zero);
+    }
+    return err;
+#else
+    (void)clear;
+    return cudaSuccess;
+#endif
+}
 
 int fused_max_cluster() {
     constexpr int kMaxDevices = 64;

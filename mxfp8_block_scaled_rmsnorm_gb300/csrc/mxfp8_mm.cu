@@ -176,14 +176,15 @@ int mm_mxfp8_static(const void* x, int64_t M, int64_t K, const void* w_q, const 
 
 int64_t mxfp8_device_status(int clear) {
     mx::set_error(MXFP8_OK, "");
-    unsigned long long st = 0;
-    const int err = mx::gemm_status(clear != 0, &st);
+    unsigned long long gemm = 0, bounds = 0;
+    int err = mx::gemm_status(clear != 0, &gemm);
+    if (err == cudaSuccess) err = mx::bounds_status(clear != 0, &bounds);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return mx::set_error(MXFP8_ERR_CUDA, "cannot read the device status: %s",
                              cudaGetErrorString(static_cast<cudaError_t>(err)));
     }
-    return (int64_t)st;
+    return (int64_t)(gemm != 0 ? gemm : bounds);
 }
 
 }  // extern "C"

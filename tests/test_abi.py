@@ -207,3 +207,18 @@ def test_launch_error_in_the_other_calls(mx, fail_launches):
                     1 << 22, None)
     msg = L.mxfp8_last_error().decode()
     assert rc == -5 and ("invalid argument" in msg or "tensor map" in msg), msg
+
+
+def test_bounds_checking_build_is_made_and_exports_the_same_calls(mx):
+    from mxfp8_block_scaled_rmsnorm_gb300 import build
+    import subprocess
+    assert os.path.exists(build.BOUNDS_LIB_PATH)
+    B = ctypes.CDLL(build.BOUNDS_LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(B, name), name
+    # the bounds build holds the device status word of its checks; the normal
+    # build does not (its checks compile to nothing)
+    sym = lambda path: subprocess.run(["nm", "-C", path], capture_output=True,
+                                      text=True).stdout
+    assert "mx::g_bounds_status" in sym(build.BOUNDS_LIB_PATH)
+    assert "mx::g_bounds_status" not in sym(build.LIB_PATH)
