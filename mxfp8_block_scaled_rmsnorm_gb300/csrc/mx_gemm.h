@@ -11,25 +11,25 @@ namespace mx {
 
 struct GemmParams {
     CUtensorMap tma_a;     // A codes [M, K] (K-major), boxes 128 B x 128 rows, 128-byte swizzle
-    CUtensorMap tma_b;     // B codes [N, K] (K-major), boxes 128 B x 256 rows
-    const uint8_t* sfa;    // A scales, tiled GEMM-operand layout (M rows, K / 32 scale columns)
-    const uint8_t* sfb;    // B scales, same layout (N rows)
+    CUtensorMap tma_b;     // B codes [N, K] (K-major), boxes 128 B x 128 rows
+    CUtensorMap tma_sfa;   // A scales (tiled layout) as 32-bit words [M/128][K/128][128]
+    CUtensorMap tma_sfb;   // B scales, same view; boxes of two 128-row tiles
     uint16_t* out;         // bf16 [M, N], row-major
     int32_t M, N, K;
-    int32_t m_tiles, n_tiles, k_tiles;  // 128-row, 256-column and 128-byte tiles
-    int32_t sfb_row_tiles;              // 128-row scale tiles of B: ceil(N / 128)
-    int32_t num_tiles;                  // m_tiles * n_tiles output tiles
+    int32_t m_tiles, n_tiles, k_tiles;  // 256-row, 256-column and 128-byte tiles
+    int32_t num_tiles;                  // m_tiles * n_tiles output tiles (one per CTA pair)
 };
 
 // Fills p for out[M, N] = A [M, K] x B [N, K]^T (E4M3 codes with tiled UE8M0
-// scales). Returns 0, or -1 / -2 when the tensor map of A / B cannot be made
-// (a driver without cuTensorMapEncodeTiled, or an address or stride TMA
-// rejects).
+// scales). Returns 0, or -1 / -2 when a tensor map of A / B (codes or scales)
+// cannot be made (a driver without cuTensorMapEncodeTiled, or an address or
+// stride TMA rejects).
 int gemm_prepare(GemmParams* p, const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                  const uint8_t* sfb, uint16_t* out, int64_t M, int64_t N, int64_t K);
 
-// One persistent launch (one CTA per SM, at most one per output tile) on
-// `stream`; returns the cudaError_t of the launch.
+// One persistent launch (CTA pairs in clusters of two, one pair per two SMs,
+// at most one pair per output tile) on `stream`; returns the cudaError_t of
+// the launch.
 int launch_gemm(const GemmParams& p, void* stream);
 
 // The GEMM's device status word (0: no wait has given up since it was last

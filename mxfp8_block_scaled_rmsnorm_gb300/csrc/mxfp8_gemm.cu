@@ -9,29 +9,37 @@
 // and sa, sb their scale bytes in the tiled GEMM-operand layout that the
 // quantize kernels write (tiles of 128 rows x 4 scale columns, 512 bytes).
 //
-// Design (one persistent CTA per SM, output tiles of 128 x 256, K in steps of
-// 128 bytes through a 4-stage shared-memory ring):
-//  - warp 0, one thread: producer. Per K step it loads the A tile (128 rows x
-//    128 bytes) and the B tile (256 x 128) with TMA (128-byte swizzle) and the
-//    matching scale tiles (one 512-byte tile for A, two for B: they are
-//    contiguous in the tiled layout) with bulk copies, all completing on the
-//    stage's "full" mbarrier.
-//  - warp 1, one thread: MMA issuer. Per K step it copies the three scale
-//    tiles into tensor memory (tcgen05.cp 32x128b.warpx4) and issues four
-//    128 x 256 x 32 MMAs (scale byte k of each 32-bit scale word for the k-th
-//    32-element block), then commits to the stage's "empty" mbarrier; after the
-//    last K step it commits to "tmem_full".
-//  - warp 2: allocates (and at the end frees) 512 tensor-memory columns: the
-//    float32 accumulator (256 columns) and per-stage scale columns.
+// Design: pairs of CTAs on two SMs (a thread-block cluster of 2) compute
+// 256 x 256 output tiles with the two-SM form of the MMA (cta_group::2):
+// CTA r of the pair holds rows 128r .. 128r+127 of the A tile and of the B
+// tile (B split along N), and its tensor memory receives its 128 rows of the
+// float32 accumulator over all 256 columns. Per SM and K step of 128 bytes
+// that is 32 KB of operands for 128 x 256 x 128 multiply-adds (the one-SM
+// 128 x 256 form needs 48 KB, more than the operand supply delivered in the
+// time the MMAs take). Persistent: one pair per two SMs walks the tiles.
+//  - warp 0, one thread per CTA: producer. Per K step it loads its A and B
+//    halves (TMA, 128-byte swizzle) and the scale tiles (TMA over a 3-D view
+//    of the tiled scales: its own A tile, both 128-row B tiles, since its
+//    accumulator rows span all 256 columns) into a 6-stage ring. All copies
+//    of both CTAs complete on the leader CTA's "full" barrier.
+//  - warp 1 of the leader CTA, one thread: MMA issuer. Per K step it copies
+//    the scale tiles of both CTAs into their tensor memory (tcgen05.cp
+//    32x128b.warpx4) and issues four 256 x 256 x 32 MMAs (scale byte k of each
+//    32-bit scale word for the k-th 32-element block), then commits to the
+//    "empty" barrier of both CTAs; after the last K step, to "tmem_full".
+//  - warp 2 of each CTA: allocates (and at the end frees) 512 tensor-memory
+//    columns, collectively for the pair: the accumulator (256 columns) and
+//    per-stage scale columns.
 //  - warps 4-11: epilogue. Each reads its 32 accumulator lanes (its TMEM lane
 //    quarter, warp % 4) over 128 columns with tcgen05.ld, converts to bf16
-//    (round to nearest even), releases the accumulator ("tmem_empty"), then
-//    stores, so the next tile's MMAs overlap the stores.
+//    (round to nearest even), releases the accumulator (an arrival on the
+//    leader's "tmem_empty"), then stores, so the next tile's MMAs overlap the
+//    stores.
 //  - Every mbarrier wait gives up after a time limit: it records the site in a
 //    device status word (read by mxfp8_device_status), raises a CTA-wide abort
-//    flag that ends the other roles' waits, waits (bounded) for the thread's
-//    own copies and MMAs in flight, and the CTA frees its tensor memory and
-//    exits.
+//    flag that ends the CTA's other waits, the leader waits (bounded) for the
+//    pair's copies and MMAs in flight, and both CTAs meet at a cluster barrier,
+//    free their tensor memory and exit.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -48,22 +56,25 @@ __device__ unsigned long long g_gemm_status = 0;
 
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 128;  // kBK: bytes = E4M3 elements
-constexpr int kStages = 4;
+constexpr int kBM = 128;   // A rows per CTA (256 per pair)
+constexpr int kBN = 256;   // output columns per tile; B rows per CTA: kBN / 2
+constexpr int kBK = 128;   // bytes = E4M3 elements per K step
+constexpr int kStages = 6;
 constexpr int kThreads = 384;
 constexpr int kEpilogueWarp0 = 4;
-constexpr uint32_t kTileA = kBM * kBK;  // 16 KB
-constexpr uint32_t kTileB = kBN * kBK;  // 32 KB
-constexpr uint32_t kSfTile = 512;       // one 128-row x 4 scale tile
-constexpr uint32_t kSfStage = 3 * kSfTile;
+constexpr uint32_t kTileA = kBM * kBK;        // 16 KB
+constexpr uint32_t kTileB = (kBN / 2) * kBK;  // 16 KB
+constexpr uint32_t kSfTile = 512;             // one 128-row x 4 scale tile
+constexpr uint32_t kSfStage = 3 * kSfTile;    // A tile, then the two B tiles
+constexpr uint32_t kStageTx = kTileA + kTileB + kSfStage;  // bytes one CTA loads per stage
 constexpr uint32_t kOffB = kStages * kTileA;
 constexpr uint32_t kOffSf = kOffB + kStages * kTileB;
 constexpr uint32_t kOffBar = kOffSf + kStages * kSfStage;
 constexpr uint32_t kBarBytes = 256;
 constexpr uint32_t kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColSfa = kBN;                     // 4 columns per stage
-constexpr uint32_t kColSfb = kBN + 4 * kStages;       // 8 columns per stage
+constexpr uint32_t kColSfa = kBN;                // 4 columns per stage
+constexpr uint32_t kColSfb = kBN + 4 * kStages;  // 8 columns per stage
 static_assert(kColSfb + 8 * kStages <= kTmemCols, "tensor memory budget");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
@@ -78,6 +89,21 @@ enum : uint32_t { kSiteEmpty = 1, kSiteTmemEmpty = 2, kSiteFull = 3, kSiteTmemFu
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// The shared::cluster address of the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
 __device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -86,14 +112,16 @@ __device__ __forceinline__ void bar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
-__device__ __forceinline__ void bar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+// Arrival on a barrier given by its shared::cluster address (this CTA's or the peer's).
+__device__ __forceinline__ void bar_arrive_cluster(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+                 : "memory");
 }
 __device__ __forceinline__ bool bar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
         : "r"(bar), "r"(parity)
@@ -132,23 +160,22 @@ __device__ void drain_bar(uint32_t bar, uint32_t parity) {
         if (global_ns() - t0 > kWaitLimitNs) return;
 }
 
-// 2-D TMA load of one box into shared memory, completing on `bar`.
+// TMA loads into this CTA's shared memory, completing on the barrier at the
+// shared::cluster address `bar` (the leader CTA's, for both CTAs of the pair).
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
                                             int32_t y, uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
-
-// Contiguous bulk copy global -> shared (16-byte aligned, size a multiple of 16).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                            int32_t y, int32_t z, uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
 }
 
@@ -160,28 +187,31 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // Copy one 512-byte scale tile (32 rows x 16 bytes in shared memory) to four
-// tensor-memory columns, replicated into all four 32-lane quarters.
+// tensor-memory columns, replicated into all four 32-lane quarters, in both
+// CTAs of the pair (each from its own shared memory).
 __device__ __forceinline__ void tc_copy_scales(uint32_t taddr, uint64_t desc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
                  : "memory");
 }
 
-// D (+)= A x B with block scales; accumulate selects D += (else D =).
+// D (+)= A x B with block scales over the pair; accumulate selects D += (else D =).
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                        uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
         " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
         : "memory");
 }
 
-// Arrive on `bar` once every tcgen05 operation this thread issued has completed.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
+// Arrive on the barrier at offset `bar` in the CTAs of `mask` once every
+// tcgen05 operation this thread issued has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar, uint16_t mask) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar), "h"(mask)
         : "memory");
 }
 
@@ -211,11 +241,27 @@ __device__ __forceinline__ uint32_t bf16x2(uint32_t lo_f32, uint32_t hi_f32) {
     return r;
 }
 
+// Output tile t of the launch: tiles are taken in groups of kGroupN column
+// blocks, row blocks fastest within a group, so that the tiles in flight at
+// once (one per pair) share a few column blocks of B and a band of A rows,
+// which stay in L2 instead of the whole of A being re-read per column block.
+constexpr int kGroupN = 8;
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& m_pair, int& n_blk) {
+    const int per_group = kGroupN * p.m_tiles;
+    const int g = t / per_group;
+    const int first = g * kGroupN;
+    const int width = p.n_tiles - first < kGroupN ? p.n_tiles - first : kGroupN;
+    const int in = t - g * per_group;
+    n_blk = first + in % width;
+    m_pair = in / width;
+}
+
 // ----------------------------------------------------------------- kernel ---
 
 __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
-    // 128-byte-swizzled tiles must start on 1024-byte boundaries
+    // 128-byte-swizzled tiles must start on 1024-byte boundaries (the same
+    // offsets in both CTAs of the pair, as the two-SM MMA requires)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -231,57 +277,58 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
     volatile uint32_t* abort = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1, pairs = gridDim.x >> 1;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            bar_init(full(s), 1);
+            bar_init(full(s), 1);  // the leader's producer; bytes from both CTAs
             bar_init(empty(s), 1);
         }
         bar_init(tmem_full, 1);
-        bar_init(tmem_empty, 8);  // one arrival per epilogue warp
+        bar_init(tmem_empty, 16);  // one arrival per epilogue warp of the pair
         bar_init(drain, 1);
         *abort = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 2) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
                      "r"(kTmemCols)
                      : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------- producer
+        const uint32_t lead_full0 = peer_addr(full(0), 0);
         int s = 0;
         uint32_t ph = 0;
         uint32_t last_par[kStages];
         bool used[kStages];
         for (int i = 0; i < kStages; ++i) used[i] = false;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-            const int m_blk = tile % p.m_tiles, n_blk = tile / p.m_tiles;
-            const bool second = 2 * n_blk + 1 < p.sfb_row_tiles;
-            const uint32_t tx = kTileA + kTileB + kSfTile * (second ? 3u : 2u);
+        for (int tile = pair; ok && tile < p.num_tiles; tile += pairs) {
+            int m_pair, n_blk;
+            tile_coords(p, tile, m_pair, n_blk);
+            const int m_tile = 2 * m_pair + (int)rank;  // this CTA's 128-row tile of A
             for (int kt = 0; kt < p.k_tiles; ++kt) {
                 if (!wait_bar(empty(s), ph ^ 1u, abort, kSiteEmpty)) {
                     ok = false;
                     break;
                 }
-                bar_expect_tx(full(s), tx);
-                tma_load_2d(sbase + s * kTileA, &p.tma_a, kt * kBK, m_blk * kBM, full(s));
-                tma_load_2d(sbase + kOffB + s * kTileB, &p.tma_b, kt * kBK, n_blk * kBN, full(s));
+                if (leader) bar_expect_tx(full(s), 2 * kStageTx);
+                const uint32_t fb = lead_full0 + 8u * (uint32_t)s;
                 const uint32_t sf = sbase + kOffSf + s * kSfStage;
-                bulk_load(sf, p.sfa + ((size_t)m_blk * p.k_tiles + kt) * kSfTile, kSfTile, full(s));
-                bulk_load(sf + kSfTile, p.sfb + ((size_t)(2 * n_blk) * p.k_tiles + kt) * kSfTile,
-                          kSfTile, full(s));
-                if (second)
-                    bulk_load(sf + 2 * kSfTile,
-                              p.sfb + ((size_t)(2 * n_blk + 1) * p.k_tiles + kt) * kSfTile,
-                              kSfTile, full(s));
+                tma_load_2d(sbase + s * kTileA, &p.tma_a, kt * kBK, m_tile * kBM, fb);
+                tma_load_2d(sbase + kOffB + s * kTileB, &p.tma_b, kt * kBK,
+                            n_blk * kBN + (int)rank * (kBN / 2), fb);
+                tma_load_3d(sf, &p.tma_sfa, 0, kt, m_tile, fb);
+                tma_load_3d(sf + kSfTile, &p.tma_sfb, 0, kt, 2 * n_blk, fb);
                 used[s] = true;
                 last_par[s] = ph;
                 if (++s == kStages) {
@@ -299,18 +346,20 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
                     ph ^= 1u;
                 }
             }
-        } else {
-            // gave up: the copies already issued land before the CTA exits
+        } else if (leader) {
+            // gave up: the pair's copies already issued land (the leader's full
+            // barriers count both CTAs' bytes) before either CTA exits
             for (int i = 0; i < kStages; ++i)
                 if (used[i]) drain_bar(full(i), last_par[i]);
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1 && lane == 0 && leader) {
         // ---------------------------------------------------- MMA issuer
         int s = 0;
         uint32_t ph = 0, local = 0;
         bool ok = true;
         const uint32_t acc = tmem;  // lane 0, column 0
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+        const uint32_t idesc0 = umma::idesc_mxf8(2 * kBM, kBN, 0, 0);
+        for (int tile = pair; ok && tile < p.num_tiles; tile += pairs, ++local) {
             if (!wait_bar(tmem_empty, (local & 1u) ^ 1u, abort, kSiteTmemEmpty)) {
                 ok = false;
                 break;
@@ -335,30 +384,32 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
                 for (int k = 0; k < nk; ++k) {
                     tc_mma(acc, umma::kmajor_sw128_desc(a0 + 32u * k),
                            umma::kmajor_sw128_desc(b0 + 32u * k),
-                           umma::idesc_mxf8(kBM, kBN, (uint32_t)k, (uint32_t)k), t_sfa, t_sfb,
+                           idesc0 | ((uint32_t)k << 29) | ((uint32_t)k << 4), t_sfa, t_sfb,
                            (kt | k) != 0 ? 1u : 0u);
                 }
-                tc_commit(empty(s));
+                tc_commit(empty(s), 3);
                 if (++s == kStages) {
                     s = 0;
                     ph ^= 1u;
                 }
             }
             if (!ok) break;
-            tc_commit(tmem_full);
+            tc_commit(tmem_full, 3);
         }
         if (!ok) {
-            // gave up: let this thread's MMAs and scale copies finish first
-            tc_commit(drain);
+            // gave up: let the pair's MMAs and scale copies finish first
+            tc_commit(drain, 1);
             drain_bar(drain, 0);
         }
     } else if (warp >= kEpilogueWarp0) {
         // ---------------------------------------------------- epilogue
-        const int quarter = warp & 3;                       // TMEM lanes 32q .. 32q+31
-        const int half = (warp - kEpilogueWarp0) >> 2;      // accumulator columns 128h ..
+        const int quarter = warp & 3;                   // TMEM lanes 32q .. 32q+31
+        const int half = (warp - kEpilogueWarp0) >> 2;  // accumulator columns 128h ..
+        const uint32_t lead_tmem_empty = peer_addr(tmem_empty, 0);
         uint32_t local = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
-            const int m_blk = tile % p.m_tiles, n_blk = tile / p.m_tiles;
+        for (int tile = pair; tile < p.num_tiles; tile += pairs, ++local) {
+            int m_pair, n_blk;
+            tile_coords(p, tile, m_pair, n_blk);
             // every lane waits; the warp goes on (converged, as the .sync.aligned
             // tensor-memory loads need) only if all lanes saw the phase complete
             const bool ok = wait_bar(tmem_full, local & 1u, abort, kSiteTmemFull);
@@ -375,8 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) bar_arrive(tmem_empty);
-            const int64_t row = (int64_t)m_blk * kBM + 32 * quarter + lane;
+            if (lane == 0) bar_arrive_cluster(lead_tmem_empty);
+            const int64_t row = (int64_t)(2 * m_pair + (int)rank) * kBM + 32 * quarter + lane;
             const int64_t col0 = (int64_t)n_blk * kBN + 128 * half;
             if (row < p.M) {
                 uint16_t* o = p.out + row * p.N + col0;
@@ -390,11 +441,12 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
         }
     }
 
+    // both CTAs done with the pair's barriers and tensor memory
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     if (warp == 2) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols)
                      : "memory");
     }
@@ -424,18 +476,36 @@ EncodeTiled encoder() {
 }
 
 // Tensor map of a K-major E4M3 operand [rows, K]: boxes of 128 bytes of K by
-// box_rows rows, 128-byte swizzle, zero fill outside the matrix.
-int encode_operand(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
-                   uint32_t box_rows) {
+// 128 rows, 128-byte swizzle, zero fill outside the matrix.
+int encode_operand(CUtensorMap* map, const void* base, int64_t rows, int64_t K) {
     EncodeTiled fn = encoder();
     if (fn == nullptr) return -1;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)K};
-    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, 128};
     const cuuint32_t elem[2] = {1, 1};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                           strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : (int)r;
+}
+
+// Tensor map of tiled scales (an operand with `rows` rows and K / 32 scale
+// columns) as a 3-D array of 32-bit words: [128-row tiles][K steps][128 words],
+// each innermost row one 512-byte scale tile; boxes of `tiles` 128-row tiles
+// at one K step, zero fill past the last row tile.
+int encode_scales(CUtensorMap* map, const void* base, int64_t rows, int64_t k_tiles,
+                  uint32_t tiles) {
+    EncodeTiled fn = encoder();
+    if (fn == nullptr) return -1;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)k_tiles, (cuuint64_t)((rows + 127) / 128)};
+    const cuuint64_t strides[2] = {kSfTile, (cuuint64_t)k_tiles * kSfTile};
+    const cuuint32_t box[3] = {128, 1, tiles};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims,
+                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? 0 : (int)r;
 }
@@ -446,48 +516,59 @@ constexpr int kMaxDevices = 64;
 
 int gemm_prepare(GemmParams* p, const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                  const uint8_t* sfb, uint16_t* out, int64_t M, int64_t N, int64_t K) {
-    if (encode_operand(&p->tma_a, a, M, K, kBM) != 0) return -1;
-    if (encode_operand(&p->tma_b, b, N, K, kBN) != 0) return -2;
-    p->sfa = sfa;
-    p->sfb = sfb;
+    const int64_t k_tiles = (K + kBK - 1) / kBK;
+    if (encode_operand(&p->tma_a, a, M, K) != 0 || encode_scales(&p->tma_sfa, sfa, M, k_tiles, 1))
+        return -1;
+    if (encode_operand(&p->tma_b, b, N, K) != 0 || encode_scales(&p->tma_sfb, sfb, N, k_tiles, 2))
+        return -2;
     p->out = out;
     p->M = (int32_t)M;
     p->N = (int32_t)N;
     p->K = (int32_t)K;
-    p->m_tiles = (int32_t)((M + kBM - 1) / kBM);
+    p->m_tiles = (int32_t)((M + 2 * kBM - 1) / (2 * kBM));
     p->n_tiles = (int32_t)((N + kBN - 1) / kBN);
-    p->k_tiles = (int32_t)((K + kBK - 1) / kBK);
-    p->sfb_row_tiles = (int32_t)((N + 127) / 128);
+    p->k_tiles = (int32_t)k_tiles;
     p->num_tiles = p->m_tiles * p->n_tiles;
     return 0;
 }
 
 int launch_gemm(const GemmParams& p, void* stream) {
     if (const int e = hook_launch_error()) return e;
-    static int sms[kMaxDevices] = {0};
-    static bool attr[kMaxDevices] = {false};
+    // pairs the device holds at once (the persistent grid: a pair that had to
+    // wait for another to finish would run its whole share of tiles late)
+    static int resident[kMaxDevices] = {0};
     int dev = 0;
     int err = (int)cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
-    if (!attr[dev]) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attrs[1];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = 2;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 1;
+    if (resident[dev] == 0) {
         err = (int)cudaFuncSetAttribute(mxfp8_gemm_kernel,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)kSmemBytes);
         if (err != cudaSuccess) return err;
-        err = (int)cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        int sms = 0, clusters = 0;
+        err = (int)cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (err != cudaSuccess) return err;
-        attr[dev] = true;
+        cfg.gridDim = dim3((unsigned)(sms & ~1), 1, 1);
+        err = (int)cudaOccupancyMaxActiveClusters(&clusters, mxfp8_gemm_kernel, &cfg);
+        if (err != cudaSuccess) return err;
+        if (clusters < 1) return (int)cudaErrorInvalidConfiguration;
+        resident[dev] = clusters;
     }
-    const int grid = p.num_tiles < sms[dev] ? p.num_tiles : sms[dev];
-    if (grid <= 0) return cudaSuccess;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = static_cast<cudaStream_t>(stream);
-    cfg.numAttrs = 0;
-    cfg.attrs = nullptr;
+    const int pairs = p.num_tiles < resident[dev] ? p.num_tiles : resident[dev];
+    if (pairs <= 0) return cudaSuccess;
+    cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
     return (int)cudaLaunchKernelEx(&cfg, mxfp8_gemm_kernel, p);
 }
 
