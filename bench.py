@@ -448,9 +448,9 @@ def run_mm(args, world, rank, local, pg):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
             "config": {"workload": f"mm_mxfp8-{M}x{N}x{K}", "M": M, "N": N, "K": K,
-                       "gemm": "mxfp8_gemm_kernel: tcgen05 kind::mxf8f6f4 block-scaled "
-                               "(E4M3 x E4M3, UE8M0 per 32), 128x256 tiles, float32 "
-                               "accumulation in tensor memory, bf16 out",
+                       "gemm": "mxfp8_gemm_kernel: tcgen05 cta_group::2 kind::mxf8f6f4 "
+                               "block-scaled (E4M3 x E4M3, UE8M0 per 32), 256x256 tiles per "
+                               "CTA pair, float32 accumulation in tensor memory, bf16 out",
                        "l2": ("operands fit in L2 (%.0f MB): a 256 MB memset and a 256 MB "
                               "read flush L2 before every timed launch, outside its events"
                               % (in_bytes / 1e6)
