@@ -1,6 +1,7 @@
 """GPU: the MXFP8 matrix multiply consumer (x quantized on the fly, weight
-pre-quantized, cuBLASLt block-scaled GEMM) against the oracle's float64 value
-of the same quantized product.
+pre-quantized, this library's tcgen05 block-scaled GEMM) against the oracle's
+float64 value of the same quantized product. After every product the
+library's device status must read 0 (no wait of the GEMM's pipeline gave up).
 
 Tolerance, elementwise: |out - ref| <= 2^-8 |ref| + 2^-16 (|A| |B|^T): one bf16
 rounding of the output plus float32 accumulation. A different activation
@@ -44,6 +45,32 @@ def test_mm_matches_oracle(M, N, K):
     got = out.float().cpu().numpy().astype(np.float64)
     ref = oracle.mm_mxfp8(x, w)
     bound = 2.0**-8 * np.abs(ref) + 2.0**-16 * _abs_bound(x, w) + 1e-30
+    assert np.all(np.abs(got - ref) <= bound), float(np.max(np.abs(got - ref) / bound))
+    assert mx.device_status() == 0
+
+
+@pytest.mark.slow
+def test_mm_full_size_sampled_rows():
+    """8192 x 14336 x 4096, the shape bench.py --mm times, in the same launch
+    configuration (one persistent grid of CTA pairs walking 1792 tiles): up to
+    128 sampled rows (the first and last rows of the first and last 256-row
+    tiles, and random ones) of the whole output against the oracle."""
+    M, N, K = 8192, 14336, 4096
+    rng = np.random.default_rng(7)
+    x = W.to_bf16_bits(rng.standard_normal((M, K), dtype=np.float32))
+    w = W.to_bf16_bits(0.02 * rng.standard_normal((N, K), dtype=np.float32))
+    wq = mx.quantize_weight_for_mm(to_dev(w))
+    out = mx.mm_mxfp8(to_dev(x), wq.q_row, wq.s_row)
+    sync()
+    assert mx.device_status() == 0
+    rows = np.unique(np.concatenate([[0, 127, 128, 255, M - 256, M - 129, M - 128, M - 1],
+                                     rng.choice(M, 120, replace=False)]))
+    got = out[torch.from_numpy(rows).to(out.device)].double().cpu().numpy()
+    qx, sx, _, _ = oracle.quant_mxfp8(np.ascontiguousarray(x[rows]), True, False, threads=None)
+    qw, sw, _, _ = oracle.quant_mxfp8(w, True, False, threads=None)
+    A, B = oracle.dequantize_rowwise(qx, sx), oracle.dequantize_rowwise(qw, sw)
+    ref = A @ B.T
+    bound = 2.0**-8 * np.abs(ref) + 2.0**-16 * (np.abs(A) @ np.abs(B).T) + 1e-30
     assert np.all(np.abs(got - ref) <= bound), float(np.max(np.abs(got - ref) / bound))
 
 
