@@ -40,9 +40,11 @@
  * Conventions for every call
  * --------------------------
  *  - All buffers are DEVICE memory of the current device, owned by the caller;
- *    the library allocates no memory and never synchronizes. Outputs are
- *    overwritten in place, so pointers captured in a CUDA graph stay valid
- *    (the inference page, `quantize_params_to_mxfp8`, persistent buffers).
+ *    the library allocates no memory and never synchronizes (except
+ *    mxfp8_device_status). Outputs are overwritten in place, so a capture of
+ *    the quantize calls in a CUDA graph stays valid across replays on the same
+ *    buffers (the inference page, `quantize_params_to_mxfp8`, persistent
+ *    buffers).
  *  - Matrices are dense row-major: element (r, c) at index r * cols + c.
  *  - Every pointer that a call uses must be non-NULL and 16-byte aligned.
  *    Pointers of disabled planes are ignored and may be NULL.
