@@ -15,8 +15,8 @@
 // tile (B split along N), and its tensor memory receives its 128 rows of the
 // float32 accumulator over all 256 columns. Per SM and K step of 128 bytes
 // that is 32 KB of operands for 128 x 256 x 128 multiply-adds (the one-SM
-// 128 x 256 form needs 48 KB, more than the operand supply delivered in the
-// time the MMAs take). Persistent: one pair per two SMs walks the tiles.
+// 128 x 256 form moves 48 KB). Persistent: the pairs the device holds at once
+// walk the output tiles.
 //  - warp 0, one thread per CTA: producer. Per K step it loads its A and B
 //    halves (TMA, 128-byte swizzle) and the scale tiles (TMA over a 3-D view
 //    of the tiled scales: its own A tile, both 128-row B tiles, since its

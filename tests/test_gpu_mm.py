@@ -35,7 +35,10 @@ def _abs_bound(x, w):
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 384, 1024), (200, 128, 512), (1, 16, 32),
-                                   (33, 256, 7168), (1024, 4096, 4096)])
+                                   (33, 256, 7168), (1024, 4096, 4096),
+                                   # ragged in all three: partial 256-row and
+                                   # 256-column tiles, K % 128 == 32, many pairs
+                                   (1000, 2064, 4000), (200, 272, 1056)])
 def test_mm_matches_oracle(M, N, K):
     x = W.random_fused(M, K, seed=M + K, scale=2.0).tensors[0].x
     w = W.random_weights([(N, K)], seed=N + K).tensors[0].x
