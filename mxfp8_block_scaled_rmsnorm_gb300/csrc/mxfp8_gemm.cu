@@ -137,8 +137,10 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Waits until the phase of `bar` with parity `parity` has completed. Gives up
 // after kWaitLimitNs (recording `site` and raising the abort flag), or as soon
 // as another thread of the CTA has given up. Returns whether the phase completed.
-__device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort, uint32_t site) {
-    if (bar_try_wait(bar, parity)) return true;
+// The first poll is inline (the common case in the MMA thread's loop, whose
+// issue rate bounds the tensor pipe); the rest is an out-of-line call.
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
+                                           uint32_t site) {
     const uint64_t t0 = global_ns();
     while (true) {
         for (int i = 0; i < 32; ++i)
@@ -150,6 +152,10 @@ __device__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort
             return false;
         }
     }
+}
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
+                                         uint32_t site) {
+    return bar_try_wait(bar, parity) || wait_bar_slow(bar, parity, abort, site);
 }
 
 // The same wait, used while draining after an abort: bounded, and not cut
@@ -192,6 +198,11 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tc_copy_scales(uint32_t taddr, uint64_t desc) {
     asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
                  : "memory");
+}
+
+// A 64-bit descriptor from its two 32-bit words.
+__device__ __forceinline__ uint64_t desc64(uint32_t lo, uint32_t hi) {
+    return ((uint64_t)hi << 32) | lo;
 }
 
 // D (+)= A x B with block scales over the pair; accumulate selects D += (else D =).
@@ -308,9 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
         const uint32_t lead_full0 = peer_addr(full(0), 0);
         int s = 0;
         uint32_t ph = 0;
-        uint32_t last_par[kStages];
-        bool used[kStages];
-        for (int i = 0; i < kStages; ++i) used[i] = false;
+        uint32_t used = 0, last_par = 0;  // per stage: filled at all; parity of its last fill
         bool ok = true;
         for (int tile = pair; ok && tile < p.num_tiles; tile += pairs) {
             int m_pair, n_blk;
@@ -329,8 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
                             n_blk * kBN + (int)rank * (kBN / 2), fb);
                 tma_load_3d(sf, &p.tma_sfa, 0, kt, m_tile, fb);
                 tma_load_3d(sf + kSfTile, &p.tma_sfb, 0, kt, 2 * n_blk, fb);
-                used[s] = true;
-                last_par[s] = ph;
+                used |= 1u << s;
+                last_par = (last_par & ~(1u << s)) | (ph << s);
                 if (++s == kStages) {
                     s = 0;
                     ph ^= 1u;
@@ -350,15 +359,28 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
             // gave up: the pair's copies already issued land (the leader's full
             // barriers count both CTAs' bytes) before either CTA exits
             for (int i = 0; i < kStages; ++i)
-                if (used[i]) drain_bar(full(i), last_par[i]);
+                if ((used >> i) & 1u) drain_bar(full(i), (last_par >> i) & 1u);
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ---------------------------------------------------- MMA issuer
+        // One thread feeds the tensor pipe, so its loop is kept short: the
+        // descriptors of stage s and K offset k are precomputed words plus
+        // constants (a descriptor's start field is the shared-memory address
+        // >> 4 in its low bits; the other fields are the same for every tile
+        // of a kind, and the addresses stay below 2^18, so adds never carry
+        // out of the field).
         int s = 0;
         uint32_t ph = 0, local = 0;
         bool ok = true;
         const uint32_t acc = tmem;  // lane 0, column 0
+        const uint64_t da = umma::kmajor_sw128_desc(sbase);
+        const uint64_t db = umma::kmajor_sw128_desc(sbase + kOffB);
+        const uint64_t dsf = umma::scale_tile_desc(sbase + kOffSf);
+        const uint32_t a_lo0 = (uint32_t)da, op_hi = (uint32_t)(da >> 32);
+        const uint32_t b_lo0 = (uint32_t)db;
+        const uint32_t sf_lo0 = (uint32_t)dsf, sf_hi = (uint32_t)(dsf >> 32);
         const uint32_t idesc0 = umma::idesc_mxf8(2 * kBM, kBN, 0, 0);
+        const int full_steps = p.K / kBK;  // K steps with all four 32-element blocks
         for (int tile = pair; ok && tile < p.num_tiles; tile += pairs, ++local) {
             if (!wait_bar(tmem_empty, (local & 1u) ^ 1u, abort, kSiteTmemEmpty)) {
                 ok = false;
@@ -371,21 +393,27 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sf = sbase + kOffSf + s * kSfStage;
+                const uint32_t sf_lo = sf_lo0 + (uint32_t)s * (kSfStage >> 4);
                 const uint32_t t_sfa = tmem + kColSfa + 4u * s;
                 const uint32_t t_sfb = tmem + kColSfb + 8u * s;
-                tc_copy_scales(t_sfa, umma::scale_tile_desc(sf));
-                tc_copy_scales(t_sfb, umma::scale_tile_desc(sf + kSfTile));
-                tc_copy_scales(t_sfb + 4u, umma::scale_tile_desc(sf + 2 * kSfTile));
-                const int rem = (p.K - kt * kBK) / 32;
-                const int nk = rem < 4 ? rem : 4;
-                const uint32_t a0 = sbase + s * kTileA;
-                const uint32_t b0 = sbase + kOffB + s * kTileB;
-                for (int k = 0; k < nk; ++k) {
-                    tc_mma(acc, umma::kmajor_sw128_desc(a0 + 32u * k),
-                           umma::kmajor_sw128_desc(b0 + 32u * k),
-                           idesc0 | ((uint32_t)k << 29) | ((uint32_t)k << 4), t_sfa, t_sfb,
-                           (kt | k) != 0 ? 1u : 0u);
+                tc_copy_scales(t_sfa, desc64(sf_lo, sf_hi));
+                tc_copy_scales(t_sfb, desc64(sf_lo + (kSfTile >> 4), sf_hi));
+                tc_copy_scales(t_sfb + 4u, desc64(sf_lo + 2 * (kSfTile >> 4), sf_hi));
+                const uint32_t a_lo = a_lo0 + (uint32_t)s * (kTileA >> 4);
+                const uint32_t b_lo = b_lo0 + (uint32_t)s * (kTileB >> 4);
+                if (kt < full_steps) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        tc_mma(acc, desc64(a_lo + 2u * k, op_hi), desc64(b_lo + 2u * k, op_hi),
+                               idesc0 | ((uint32_t)k << 29) | ((uint32_t)k << 4), t_sfa, t_sfb,
+                               (kt | k) != 0 ? 1u : 0u);
+                } else {
+                    // the last, partial K step: only the 32-element blocks that exist
+                    const int nk = (p.K - kt * kBK) / 32;
+                    for (int k = 0; k < nk; ++k)
+                        tc_mma(acc, desc64(a_lo + 2u * k, op_hi), desc64(b_lo + 2u * k, op_hi),
+                               idesc0 | ((uint32_t)k << 29) | ((uint32_t)k << 4), t_sfa, t_sfb,
+                               (kt | k) != 0 ? 1u : 0u);
                 }
                 tc_commit(empty(s), 3);
                 if (++s == kStages) {
