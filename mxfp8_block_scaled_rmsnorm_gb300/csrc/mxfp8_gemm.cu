@@ -22,11 +22,17 @@
 //    of the tiled scales: its own A tile, both 128-row B tiles, since its
 //    accumulator rows span all 256 columns) into a 6-stage ring. All copies
 //    of both CTAs complete on the leader CTA's "full" barrier.
-//  - warp 1 of the leader CTA, one thread: MMA issuer. Per K step it copies
-//    the scale tiles of both CTAs into their tensor memory (tcgen05.cp
-//    32x128b.warpx4) and issues four 256 x 256 x 32 MMAs (scale byte k of each
-//    32-bit scale word for the k-th 32-element block), then commits to the
-//    "empty" barrier of both CTAs; after the last K step, to "tmem_full".
+//  - warp 3 of the leader CTA, one thread: scale copier. As soon as a stage
+//    lands it copies the stage's scale tiles of both CTAs into their tensor
+//    memory (tcgen05.cp 32x128b.warpx4, one column slot per stage) and
+//    commits to the stage's "sf_full" barrier.
+//  - warp 1 of the leader CTA, one thread: MMA issuer. Per K step it issues
+//    four 256 x 256 x 32 MMAs (scale byte k of each 32-bit scale word for the
+//    k-th 32-element block), then commits to the "empty" barrier of both
+//    CTAs; after the last K step, to "tmem_full". One thread feeds the tensor
+//    pipe, so its loop is kept to these instructions: each tcgen05 issue costs
+//    the thread tens of cycles, and with the scale copies and full descriptor
+//    arithmetic on the same thread the pipe idled half of the time.
 //  - warp 2 of each CTA: allocates (and at the end frees) 512 tensor-memory
 //    columns, collectively for the pair: the accumulator (256 columns) and
 //    per-stage scale columns.
@@ -277,14 +283,17 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    // bars[0, S): full; [S, 2S): empty; 2S: tmem_full; 2S+1: tmem_empty; 2S+2: drain
+    // bars[0, S): full; [S, 2S): empty; [2S, 3S): sf_full; 3S: tmem_full;
+    // 3S+1: tmem_empty; 3S+2: drain (MMA issuer); 3S+3: drain (scale copier)
     const uint32_t bar0 = smem_u32(bars);
     auto full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
     auto empty = [&](int s) { return bar0 + 8u * (uint32_t)(kStages + s); };
-    const uint32_t tmem_full = bar0 + 8u * (2 * kStages);
-    const uint32_t tmem_empty = bar0 + 8u * (2 * kStages + 1);
-    const uint32_t drain = bar0 + 8u * (2 * kStages + 2);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * (2 * kStages + 3));
+    auto sf_full = [&](int s) { return bar0 + 8u * (uint32_t)(2 * kStages + s); };
+    const uint32_t tmem_full = bar0 + 8u * (3 * kStages);
+    const uint32_t tmem_empty = bar0 + 8u * (3 * kStages + 1);
+    const uint32_t drain = bar0 + 8u * (3 * kStages + 2);
+    const uint32_t drain_cp = bar0 + 8u * (3 * kStages + 3);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * (3 * kStages + 4));
     volatile uint32_t* abort = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -295,10 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
         for (int s = 0; s < kStages; ++s) {
             bar_init(full(s), 1);  // the leader's producer; bytes from both CTAs
             bar_init(empty(s), 1);
+            bar_init(sf_full(s), 1);
         }
         bar_init(tmem_full, 1);
         bar_init(tmem_empty, 16);  // one arrival per epilogue warp of the pair
         bar_init(drain, 1);
+        bar_init(drain_cp, 1);
         *abort = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -375,10 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
         const uint32_t acc = tmem;  // lane 0, column 0
         const uint64_t da = umma::kmajor_sw128_desc(sbase);
         const uint64_t db = umma::kmajor_sw128_desc(sbase + kOffB);
-        const uint64_t dsf = umma::scale_tile_desc(sbase + kOffSf);
         const uint32_t a_lo0 = (uint32_t)da, op_hi = (uint32_t)(da >> 32);
         const uint32_t b_lo0 = (uint32_t)db;
-        const uint32_t sf_lo0 = (uint32_t)dsf, sf_hi = (uint32_t)(dsf >> 32);
         const uint32_t idesc0 = umma::idesc_mxf8(2 * kBM, kBN, 0, 0);
         const int full_steps = p.K / kBK;  // K steps with all four 32-element blocks
         for (int tile = pair; ok && tile < p.num_tiles; tile += pairs, ++local) {
@@ -388,17 +397,16 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
             }
             tc_fence_after();
             for (int kt = 0; kt < p.k_tiles; ++kt) {
-                if (!wait_bar(full(s), ph, abort, kSiteFull)) {
+                // the stage's operands (complete by now: the copier waited for
+                // them) and its scales in tensor memory
+                if (!wait_bar(full(s), ph, abort, kSiteFull) ||
+                    !wait_bar(sf_full(s), ph, abort, kSiteFull)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sf_lo = sf_lo0 + (uint32_t)s * (kSfStage >> 4);
                 const uint32_t t_sfa = tmem + kColSfa + 4u * s;
                 const uint32_t t_sfb = tmem + kColSfb + 8u * s;
-                tc_copy_scales(t_sfa, desc64(sf_lo, sf_hi));
-                tc_copy_scales(t_sfb, desc64(sf_lo + (kSfTile >> 4), sf_hi));
-                tc_copy_scales(t_sfb + 4u, desc64(sf_lo + 2 * (kSfTile >> 4), sf_hi));
                 const uint32_t a_lo = a_lo0 + (uint32_t)s * (kTileA >> 4);
                 const uint32_t b_lo = b_lo0 + (uint32_t)s * (kTileB >> 4);
                 if (kt < full_steps) {
@@ -428,6 +436,42 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
             // gave up: let the pair's MMAs and scale copies finish first
             tc_commit(drain, 1);
             drain_bar(drain, 0);
+        }
+    } else if (warp == 3 && lane == 0 && leader) {
+        // ---------------------------------------------------- scale copier
+        // Copies each stage's scale tiles into tensor memory as soon as the
+        // stage lands, ahead of the MMAs, so that the MMA thread issues only
+        // MMAs and commits. Slot s of the scale columns is rewritten only
+        // after the stage's next fill has landed, which the producer starts
+        // only after the MMAs that read the slot have completed.
+        const uint64_t dsf = umma::scale_tile_desc(sbase + kOffSf);
+        const uint32_t sf_lo0 = (uint32_t)dsf, sf_hi = (uint32_t)(dsf >> 32);
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int tile = pair; ok && tile < p.num_tiles; tile += pairs) {
+            for (int kt = 0; kt < p.k_tiles; ++kt) {
+                if (!wait_bar(full(s), ph, abort, kSiteFull)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sf_lo = sf_lo0 + (uint32_t)s * (kSfStage >> 4);
+                const uint32_t t_sfb = tmem + kColSfb + 8u * s;
+                tc_copy_scales(tmem + kColSfa + 4u * s, desc64(sf_lo, sf_hi));
+                tc_copy_scales(t_sfb, desc64(sf_lo + (kSfTile >> 4), sf_hi));
+                tc_copy_scales(t_sfb + 4u, desc64(sf_lo + 2 * (kSfTile >> 4), sf_hi));
+                tc_commit(sf_full(s), 1);
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            // gave up: let the copies in flight finish first
+            tc_commit(drain_cp, 1);
+            drain_bar(drain_cp, 0);
         }
     } else if (warp >= kEpilogueWarp0) {
         // ---------------------------------------------------- epilogue
