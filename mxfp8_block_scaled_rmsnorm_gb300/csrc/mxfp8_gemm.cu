@@ -17,25 +17,30 @@
 // that is 32 KB of operands for 128 x 256 x 128 multiply-adds (the one-SM
 // 128 x 256 form moves 48 KB). Persistent: the pairs the device holds at once
 // walk the output tiles.
-//  - warp 0, one thread per CTA: producer. Per K step it loads its A and B
+// The issuing roles below are whole warps: every lane runs the role's loop
+// (barrier waits, stage counters, descriptor words: the same value in each
+// lane) and one elected lane issues the TMA, tcgen05 and commit instructions.
+// Kept warp-uniform, those operands need no per-instruction conversion from
+// per-thread registers; the same loops run on one thread (lane 0 alone)
+// issued 6-8 % slower over the whole GEMM.
+//  - warp 0 of each CTA: producer. Per K step it loads its A and B
 //    halves (TMA, 128-byte swizzle) and the scale tiles (TMA over a 3-D view
 //    of the tiled scales: its own A tile, both 128-row B tiles, since its
 //    accumulator rows span all 256 columns) into a 6-stage ring. All copies
 //    of both CTAs complete on the leader CTA's "full" barrier.
-//  - warp 3 of the leader CTA, one thread: scale copier. As soon as a stage
-//    lands it copies the stage's scale tiles of both CTAs into their tensor
-//    memory (tcgen05.cp 32x128b.warpx4, one column slot per stage) and
-//    commits to the stage's "sf_full" barrier.
-//  - warp 1 of the leader CTA, one thread: MMA issuer. Per K step it issues
-//    four 256 x 256 x 32 MMAs (scale byte k of each 32-bit scale word for the
-//    k-th 32-element block), then commits to the "empty" barrier of both
-//    CTAs; after the last K step, to "tmem_full". One thread feeds the tensor
-//    pipe, so its loop is kept to these instructions: each tcgen05 issue costs
-//    the thread tens of cycles, and with the scale copies and full descriptor
-//    arithmetic on the same thread the pipe idled half of the time.
+//  - warp 1 of the leader CTA: MMA issuer. Per K step it copies the stage's
+//    scale tiles of both CTAs into their tensor memory (tcgen05.cp
+//    32x128b.warpx4, one column slot per stage), issues four 256 x 256 x 32
+//    MMAs (scale byte k of each 32-bit scale word for the k-th 32-element
+//    block), then commits to the "empty" barrier of both CTAs; after the last
+//    K step, to "tmem_full". A scale copy and the MMAs after it, issued by
+//    the same thread, run in issue order on the tensor pipe, so the MMAs need
+//    no wait for the copy. The loop is kept to these instructions and
+//    precomputed descriptor words: each tcgen05 issue costs the issuing lane
+//    tens of cycles.
 //  - warp 2 of each CTA: allocates (and at the end frees) 512 tensor-memory
 //    columns, collectively for the pair: the accumulator (256 columns) and
-//    per-stage scale columns.
+//    per-stage scale columns. Warp 3 has no role.
 //  - warps 4-11: epilogue. Each reads its 32 accumulator lanes (its TMEM lane
 //    quarter, warp % 4) over 128 columns with tcgen05.ld, converts to bf16
 //    (round to nearest even), releases the accumulator (an arrival on the
@@ -78,6 +83,7 @@ constexpr uint32_t kOffSf = kOffB + kStages * kTileB;
 constexpr uint32_t kOffBar = kOffSf + kStages * kSfStage;
 constexpr uint32_t kBarBytes = 256;
 constexpr uint32_t kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
+static_assert(8 * (2 * kStages + 3) + 8 <= kBarBytes, "barriers, tensor-memory slot, abort flag");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColSfa = kBN;                // 4 columns per stage
 constexpr uint32_t kColSfb = kBN + 4 * kStages;  // 8 columns per stage
@@ -143,7 +149,7 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Waits until the phase of `bar` with parity `parity` has completed. Gives up
 // after kWaitLimitNs (recording `site` and raising the abort flag), or as soon
 // as another thread of the CTA has given up. Returns whether the phase completed.
-// The first poll is inline (the common case in the MMA thread's loop, whose
+// The first poll is inline (the common case in the MMA warp's loop, whose
 // issue rate bounds the tensor pipe); the rest is an out-of-line call.
 __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
                                            uint32_t site) {
@@ -162,6 +168,25 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volati
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
                                          uint32_t site) {
     return bar_try_wait(bar, parity) || wait_bar_slow(bar, parity, abort, site);
+}
+
+
+// The lowest lane of a converged warp, which issues the warp's tensor-core and
+// TMA operations (always the same lane, so its commits cover its own MMAs and
+// copies); the rest of the warp keeps the loop's values warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r));
+    return r != 0;
+}
+// wait_bar by every lane of a converged warp, with the same result in all lanes.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
+                                              volatile uint32_t* abort, uint32_t site) {
+    return __all_sync(0xFFFFFFFFu, wait_bar(bar, parity, abort, site));
 }
 
 // The same wait, used while draining after an abort: bounded, and not cut
@@ -283,17 +308,15 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    // bars[0, S): full; [S, 2S): empty; [2S, 3S): sf_full; 3S: tmem_full;
-    // 3S+1: tmem_empty; 3S+2: drain (MMA issuer); 3S+3: drain (scale copier)
+    // bars[0, S): full; [S, 2S): empty; 2S: tmem_full; 2S+1: tmem_empty;
+    // 2S+2: drain (MMA issuer)
     const uint32_t bar0 = smem_u32(bars);
     auto full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
     auto empty = [&](int s) { return bar0 + 8u * (uint32_t)(kStages + s); };
-    auto sf_full = [&](int s) { return bar0 + 8u * (uint32_t)(2 * kStages + s); };
-    const uint32_t tmem_full = bar0 + 8u * (3 * kStages);
-    const uint32_t tmem_empty = bar0 + 8u * (3 * kStages + 1);
-    const uint32_t drain = bar0 + 8u * (3 * kStages + 2);
-    const uint32_t drain_cp = bar0 + 8u * (3 * kStages + 3);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * (3 * kStages + 4));
+    const uint32_t tmem_full = bar0 + 8u * (2 * kStages);
+    const uint32_t tmem_empty = bar0 + 8u * (2 * kStages + 1);
+    const uint32_t drain = bar0 + 8u * (2 * kStages + 2);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * (2 * kStages + 3));
     volatile uint32_t* abort = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -304,12 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
         for (int s = 0; s < kStages; ++s) {
             bar_init(full(s), 1);  // the leader's producer; bytes from both CTAs
             bar_init(empty(s), 1);
-            bar_init(sf_full(s), 1);
         }
         bar_init(tmem_full, 1);
         bar_init(tmem_empty, 16);  // one arrival per epilogue warp of the pair
         bar_init(drain, 1);
-        bar_init(drain_cp, 1);
         *abort = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -325,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
         // ---------------------------------------------------- producer
         const uint32_t lead_full0 = peer_addr(full(0), 0);
         int s = 0;
@@ -337,18 +358,21 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
             tile_coords(p, tile, m_pair, n_blk);
             const int m_tile = 2 * m_pair + (int)rank;  // this CTA's 128-row tile of A
             for (int kt = 0; kt < p.k_tiles; ++kt) {
-                if (!wait_bar(empty(s), ph ^ 1u, abort, kSiteEmpty)) {
+                if (!wait_bar_warp(empty(s), ph ^ 1u, abort, kSiteEmpty)) {
                     ok = false;
                     break;
                 }
-                if (leader) bar_expect_tx(full(s), 2 * kStageTx);
                 const uint32_t fb = lead_full0 + 8u * (uint32_t)s;
                 const uint32_t sf = sbase + kOffSf + s * kSfStage;
-                tma_load_2d(sbase + s * kTileA, &p.tma_a, kt * kBK, m_tile * kBM, fb);
-                tma_load_2d(sbase + kOffB + s * kTileB, &p.tma_b, kt * kBK,
-                            n_blk * kBN + (int)rank * (kBN / 2), fb);
-                tma_load_3d(sf, &p.tma_sfa, 0, kt, m_tile, fb);
-                tma_load_3d(sf + kSfTile, &p.tma_sfb, 0, kt, 2 * n_blk, fb);
+                if (elect_one()) {
+                    if (leader) bar_expect_tx(full(s), 2 * kStageTx);
+                    tma_load_2d(sbase + s * kTileA, &p.tma_a, kt * kBK, m_tile * kBM, fb);
+                    tma_load_2d(sbase + kOffB + s * kTileB, &p.tma_b, kt * kBK,
+                                n_blk * kBN + (int)rank * (kBN / 2), fb);
+                    tma_load_3d(sf, &p.tma_sfa, 0, kt, m_tile, fb);
+                    tma_load_3d(sf + kSfTile, &p.tma_sfb, 0, kt, 2 * n_blk, fb);
+                }
+                __syncwarp();
                 used |= 1u << s;
                 last_par = (last_par & ~(1u << s)) | (ph << s);
                 if (++s == kStages) {
@@ -360,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
         if (ok) {
             // every stage's last release has arrived before the CTA may exit
             for (int i = 0; i < kStages; ++i) {
-                if (!wait_bar(empty(s), ph ^ 1u, abort, kSiteEmpty)) break;
+                if (!wait_bar_warp(empty(s), ph ^ 1u, abort, kSiteEmpty)) break;
                 if (++s == kStages) {
                     s = 0;
                     ph ^= 1u;
@@ -372,9 +396,11 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
             for (int i = 0; i < kStages; ++i)
                 if ((used >> i) & 1u) drain_bar(full(i), (last_par >> i) & 1u);
         }
-    } else if (warp == 1 && lane == 0 && leader) {
+    } else if (warp == 1 && leader) {
         // ---------------------------------------------------- MMA issuer
-        // One thread feeds the tensor pipe, so its loop is kept short: the
+        // One warp feeds the tensor pipe, so its loop is kept short. The whole
+        // warp runs it (waits, stage counters, descriptors: values the same in
+        // every lane) and one elected lane issues the MMAs and commits. The
         // descriptors of stage s and K offset k are precomputed words plus
         // constants (a descriptor's start field is the shared-memory address
         // >> 4 in its low bits; the other fields are the same for every tile
@@ -390,17 +416,16 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
         const uint32_t b_lo0 = (uint32_t)db;
         const uint32_t idesc0 = umma::idesc_mxf8(2 * kBM, kBN, 0, 0);
         const int full_steps = p.K / kBK;  // K steps with all four 32-element blocks
+        const uint64_t dsf = umma::scale_tile_desc(sbase + kOffSf);
+        const uint32_t sf_lo0 = (uint32_t)dsf, sf_hi = (uint32_t)(dsf >> 32);
         for (int tile = pair; ok && tile < p.num_tiles; tile += pairs, ++local) {
-            if (!wait_bar(tmem_empty, (local & 1u) ^ 1u, abort, kSiteTmemEmpty)) {
+            if (!wait_bar_warp(tmem_empty, (local & 1u) ^ 1u, abort, kSiteTmemEmpty)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             for (int kt = 0; kt < p.k_tiles; ++kt) {
-                // the stage's operands (complete by now: the copier waited for
-                // them) and its scales in tensor memory
-                if (!wait_bar(full(s), ph, abort, kSiteFull) ||
-                    !wait_bar(sf_full(s), ph, abort, kSiteFull)) {
+                if (!wait_bar_warp(full(s), ph, abort, kSiteFull)) {
                     ok = false;
                     break;
                 }
@@ -409,69 +434,46 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
                 const uint32_t t_sfb = tmem + kColSfb + 8u * s;
                 const uint32_t a_lo = a_lo0 + (uint32_t)s * (kTileA >> 4);
                 const uint32_t b_lo = b_lo0 + (uint32_t)s * (kTileB >> 4);
-                if (kt < full_steps) {
+                const uint32_t sf_lo = sf_lo0 + (uint32_t)s * (kSfStage >> 4);
+                if (elect_one()) {
+                    // scale slot s is free: the MMAs that last read it completed
+                    // before the producer refilled stage s
+                    tc_copy_scales(t_sfa, desc64(sf_lo, sf_hi));
+                    tc_copy_scales(t_sfb, desc64(sf_lo + (kSfTile >> 4), sf_hi));
+                    tc_copy_scales(t_sfb + 4u, desc64(sf_lo + 2 * (kSfTile >> 4), sf_hi));
+                    if (kt < full_steps) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        tc_mma(acc, desc64(a_lo + 2u * k, op_hi), desc64(b_lo + 2u * k, op_hi),
-                               idesc0 | ((uint32_t)k << 29) | ((uint32_t)k << 4), t_sfa, t_sfb,
-                               (kt | k) != 0 ? 1u : 0u);
-                } else {
-                    // the last, partial K step: only the 32-element blocks that exist
-                    const int nk = (p.K - kt * kBK) / 32;
-                    for (int k = 0; k < nk; ++k)
-                        tc_mma(acc, desc64(a_lo + 2u * k, op_hi), desc64(b_lo + 2u * k, op_hi),
-                               idesc0 | ((uint32_t)k << 29) | ((uint32_t)k << 4), t_sfa, t_sfb,
-                               (kt | k) != 0 ? 1u : 0u);
+                        for (int k = 0; k < 4; ++k)
+                            tc_mma(acc, desc64(a_lo + 2u * k, op_hi),
+                                   desc64(b_lo + 2u * k, op_hi),
+                                   idesc0 | ((uint32_t)k << 29) | ((uint32_t)k << 4), t_sfa,
+                                   t_sfb, (kt | k) != 0 ? 1u : 0u);
+                    } else {
+                        // the last, partial K step: only the 32-element blocks that exist
+                        const int nk = (p.K - kt * kBK) / 32;
+                        for (int k = 0; k < nk; ++k)
+                            tc_mma(acc, desc64(a_lo + 2u * k, op_hi),
+                                   desc64(b_lo + 2u * k, op_hi),
+                                   idesc0 | ((uint32_t)k << 29) | ((uint32_t)k << 4), t_sfa,
+                                   t_sfb, (kt | k) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(empty(s), 3);
                 }
-                tc_commit(empty(s), 3);
+                __syncwarp();
                 if (++s == kStages) {
                     s = 0;
                     ph ^= 1u;
                 }
             }
             if (!ok) break;
-            tc_commit(tmem_full, 3);
+            if (elect_one()) tc_commit(tmem_full, 3);
+            __syncwarp();
         }
         if (!ok) {
-            // gave up: let the pair's MMAs and scale copies finish first
-            tc_commit(drain, 1);
+            // gave up: let the pair's scale copies and MMAs finish first
+            if (elect_one()) tc_commit(drain, 1);
+            __syncwarp();
             drain_bar(drain, 0);
-        }
-    } else if (warp == 3 && lane == 0 && leader) {
-        // ---------------------------------------------------- scale copier
-        // Copies each stage's scale tiles into tensor memory as soon as the
-        // stage lands, ahead of the MMAs, so that the MMA thread issues only
-        // MMAs and commits. Slot s of the scale columns is rewritten only
-        // after the stage's next fill has landed, which the producer starts
-        // only after the MMAs that read the slot have completed.
-        const uint64_t dsf = umma::scale_tile_desc(sbase + kOffSf);
-        const uint32_t sf_lo0 = (uint32_t)dsf, sf_hi = (uint32_t)(dsf >> 32);
-        int s = 0;
-        uint32_t ph = 0;
-        bool ok = true;
-        for (int tile = pair; ok && tile < p.num_tiles; tile += pairs) {
-            for (int kt = 0; kt < p.k_tiles; ++kt) {
-                if (!wait_bar(full(s), ph, abort, kSiteFull)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t sf_lo = sf_lo0 + (uint32_t)s * (kSfStage >> 4);
-                const uint32_t t_sfb = tmem + kColSfb + 8u * s;
-                tc_copy_scales(tmem + kColSfa + 4u * s, desc64(sf_lo, sf_hi));
-                tc_copy_scales(t_sfb, desc64(sf_lo + (kSfTile >> 4), sf_hi));
-                tc_copy_scales(t_sfb + 4u, desc64(sf_lo + 2 * (kSfTile >> 4), sf_hi));
-                tc_commit(sf_full(s), 1);
-                if (++s == kStages) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-            }
-        }
-        if (!ok) {
-            // gave up: let the copies in flight finish first
-            tc_commit(drain_cp, 1);
-            drain_bar(drain_cp, 0);
         }
     } else if (warp >= kEpilogueWarp0) {
         // ---------------------------------------------------- epilogue
