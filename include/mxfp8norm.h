@@ -69,7 +69,7 @@
 extern "C" {
 #endif
 
-#define MXFP8_ABI_VERSION 6
+#define MXFP8_ABI_VERSION 7
 #define MXFP8_BLOCK_SIZE 32
 #define MXFP8_MAX_TENSORS 256
 #define MXFP8_MAX_UPDATE 256
@@ -213,6 +213,24 @@ int mxfp8_update_planes(const mxfp8_planes* src, const mxfp8_planes* dst, int n,
  * Errors: MXFP8_ERR_SHAPE, MXFP8_ERR_POINTER, MXFP8_ERR_CUDA (a launch the
  * runtime rejects, or a TMA tensor map the driver cannot make). */
 size_t mm_mxfp8_workspace_size(int64_t M, int64_t K);
+
+/* The GEMM of mm_mxfp8 alone, for an activation that is already quantized
+ * (for instance the rowwise plane that rmsnorm_quant_mxfp8_ex writes with
+ * MXFP8_SCALES_MMA_TILED, so that a norm + quantize feeds the matrix multiply
+ * without the bf16 being read again): out[M, N] = deq(x_q, x_s) deq(w_q, w_s)^T
+ * with deq(q, s)[r, k] = e4m3(q[r, k]) * 2^(s(r, k / 32) - 127), where
+ *   x_q  e4m3 codes [M, K] row-major;
+ *   x_s  their scales in MXFP8_SCALES_MMA_TILED layout (an operand with M rows
+ *        and K / 32 scale columns);
+ *   w_q, w_s, out  as for mm_mxfp8.
+ * One launch on `stream`, no scratch. The tiled buffers' padding (rows past M
+ * or N, scale columns past K / 32) is never read. The same kernel as the
+ * second launch of mm_mxfp8: on the same quantized operands the two give the
+ * same bytes.
+ * Requirements and errors as for mm_mxfp8 (every pointer 256-byte aligned);
+ * there is no workspace. */
+int mm_mxfp8_quantized(const void* x_q, const void* x_s, int64_t M, int64_t K, const void* w_q,
+                       const void* w_s, int64_t N, void* out, void* stream);
 int mm_mxfp8(const void* x, int64_t M, int64_t K, const void* w_q, const void* w_s, int64_t N,
              void* out, void* workspace, size_t workspace_bytes, void* stream);
 

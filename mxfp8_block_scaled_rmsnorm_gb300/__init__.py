@@ -120,6 +120,10 @@ def library() -> ctypes.CDLL:
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                       ctypes.c_void_p, ctypes.c_void_p]
         L.mm_mxfp8_static.restype = ctypes.c_int
+        L.mm_mxfp8_quantized.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                         ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+        L.mm_mxfp8_quantized.restype = ctypes.c_int
         L.mxfp8_device_status.argtypes = [ctypes.c_int]
         L.mxfp8_device_status.restype = ctypes.c_int64
         L.mxfp8_set_test_hook.argtypes = [ctypes.c_int, ctypes.c_int]
@@ -475,6 +479,36 @@ def mm_mxfp8(x: torch.Tensor, w_q: torch.Tensor, w_s: torch.Tensor, out=None,
     with _on_device(x.device):
         rc = L.mm_mxfp8(x.data_ptr(), M, K, w_q.data_ptr(), w_s.data_ptr(), N, out.data_ptr(),
                         workspace.data_ptr(), workspace.numel(), _stream_handle(stream, x.device))
+    if rc != 0:
+        raise MXFP8Error(rc, L.mxfp8_last_error().decode())
+    return out
+
+
+def mm_mxfp8_quantized(x_q: torch.Tensor, x_s: torch.Tensor, w_q: torch.Tensor,
+                       w_s: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+    """The GEMM of mm_mxfp8 alone: out[M, N] = deq(x_q, x_s) deq(w_q, w_s)^T for
+    an activation quantized beforehand (e.g. ``rmsnorm_quant_mxfp8(...,
+    scale_layout="mma")``'s ``q_row``/``s_row``); one launch, no workspace."""
+    if x_q.dim() != 2 or x_q.dtype != torch.uint8 or w_q.dim() != 2 or w_q.dtype != torch.uint8:
+        raise ValueError("x_q and w_q must be uint8 [M, K] and [N, K] codes")
+    M, K = x_q.shape
+    N = w_q.shape[0]
+    if w_q.shape[1] != K or x_s.dtype != torch.uint8 or w_s.dtype != torch.uint8:
+        raise ValueError("x_q [M, K] and w_q [N, K] must share K; scales must be uint8")
+    dev = x_q.device
+    _check_buffer(x_q, "x_q", dev, M * K, shape=(M, K))
+    _check_buffer(w_q, "w_q", dev, N * K, shape=(N, K))
+    if K % BLOCK == 0:
+        _check_buffer(x_s, "x_s", dev, _scale_numel(M, K, False, "mma"), at_least=True)
+        _check_buffer(w_s, "w_s", dev, _scale_numel(N, K, False, "mma"), at_least=True)
+    L = library()
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    else:
+        _check_buffer(out, "out", dev, M * N, shape=(M, N), dtype=torch.bfloat16)
+    with _on_device(dev):
+        rc = L.mm_mxfp8_quantized(x_q.data_ptr(), x_s.data_ptr(), M, K, w_q.data_ptr(),
+                                  w_s.data_ptr(), N, out.data_ptr(), _stream_handle(stream, dev))
     if rc != 0:
         raise MXFP8Error(rc, L.mxfp8_last_error().decode())
     return out

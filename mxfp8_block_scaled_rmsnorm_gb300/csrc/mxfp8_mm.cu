@@ -7,7 +7,8 @@
 // quantize kernel, with its scales in the tiled GEMM-operand layout, into a
 // scratch area; this library's tcgen05 block-scaled GEMM (mxfp8_gemm.cu) then
 // computes out = x_q w_q^T with float32 accumulation and a bf16 result. Two
-// launches on the caller's stream.
+// launches on the caller's stream (mm_mxfp8_quantized: the GEMM alone, on an
+// activation the caller quantized).
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -30,6 +31,12 @@ int64_t align256(int64_t v) { return (v + 255) / 256 * 256; }
 // Bytes of the quantized activation in the scratch: codes, then tiled scales.
 int64_t act_bytes(int64_t M, int64_t K) {
     return align256(M * K) + align256(ceil_div(M, 128) * 128 * ceil_div(K / 32, 4) * 4);
+}
+
+int gemm_error(int err) {
+    cudaGetLastError();
+    return mx::set_error(MXFP8_ERR_CUDA, "GEMM launch failed: %s",
+                         cudaGetErrorString(static_cast<cudaError_t>(err)));
 }
 
 // The product with a given scratch area (quantized activation: codes, then
@@ -71,12 +78,7 @@ int mm_run(const void* x, int64_t M, int64_t K, const void* w_q, const void* w_s
     }
     // 2. out = x_q w_q^T on the tensor cores
     err = mx::launch_gemm(gp, stream);
-    if (err != cudaSuccess) {
-        cudaGetLastError();
-        return mx::set_error(MXFP8_ERR_CUDA, "GEMM launch failed: %s",
-                             cudaGetErrorString(static_cast<cudaError_t>(err)));
-    }
-    return MXFP8_OK;
+    return err != cudaSuccess ? gemm_error(err) : MXFP8_OK;
 }
 
 int check_mm_args(const void* x, int64_t M, int64_t K, const void* w_q, const void* w_s,
@@ -153,6 +155,28 @@ int mm_mxfp8(const void* x, int64_t M, int64_t K, const void* w_q, const void* w
         return mx::set_error(MXFP8_ERR_SHAPE, "workspace of %zu bytes < %lld needed",
                              workspace_bytes, (long long)need_act);
     return mm_run(x, M, K, w_q, w_s, N, out, static_cast<uint8_t*>(workspace), stream);
+}
+
+int mm_mxfp8_quantized(const void* x_q, const void* x_s, int64_t M, int64_t K, const void* w_q,
+                       const void* w_s, int64_t N, void* out, void* stream) {
+    const mx::TraceRange trace("mm_mxfp8_quantized");
+    mx::set_error(MXFP8_OK, "");
+    int rc = check_mm_args(x_q, M, K, w_q, w_s, N, out);
+    if (rc != MXFP8_OK) return rc;
+    if (x_s == nullptr || (reinterpret_cast<uintptr_t>(x_s) & 255u) != 0)
+        return mx::set_error(MXFP8_ERR_POINTER, "x_s must be non-NULL and 256-byte aligned");
+    mx::GemmParams gp;
+    std::memset(&gp, 0, sizeof gp);
+    const int mr = mx::gemm_prepare(&gp, static_cast<const uint8_t*>(x_q),
+                                    static_cast<const uint8_t*>(x_s),
+                                    static_cast<const uint8_t*>(w_q),
+                                    static_cast<const uint8_t*>(w_s),
+                                    static_cast<uint16_t*>(out), M, N, K);
+    if (mr != 0)
+        return mx::set_error(MXFP8_ERR_CUDA, "cannot make the TMA tensor map of %s",
+                             mr == -1 ? "x_q" : "w_q");
+    const int err = mx::launch_gemm(gp, stream);
+    return err != cudaSuccess ? gemm_error(err) : MXFP8_OK;
 }
 
 int mm_mxfp8_static(const void* x, int64_t M, int64_t K, const void* w_q, const void* w_s,

@@ -30,7 +30,8 @@ def test_header_declares_the_calls():
     assert declared_functions() == sorted(
         ["rmsnorm_quant_mxfp8", "quant_mxfp8", "rmsnorm_quant_mxfp8_ex", "quant_mxfp8_ex",
          "add_rmsnorm_quant_mxfp8", "mxfp8_update_planes", "mm_mxfp8",
-         "mm_mxfp8_workspace_size", "mm_mxfp8_static", "mxfp8_last_error",
+         "mm_mxfp8_workspace_size", "mm_mxfp8_static", "mm_mxfp8_quantized",
+         "mxfp8_last_error",
          "mxfp8_abi_version", "mxfp8_rmsnorm_quant", "mxfp8_quant", "mxfp8_set_test_hook",
          "mxfp8_device_status"])
 
@@ -39,7 +40,7 @@ def test_library_exports_every_declared_symbol(mx):
     L = mx.library()
     for name in declared_functions():
         assert hasattr(L, name), name
-    assert L.mxfp8_abi_version() == 6
+    assert L.mxfp8_abi_version() == 7
 
 
 def test_desc_struct_layout_matches_header(mx):
@@ -207,6 +208,27 @@ def test_launch_error_in_the_other_calls(mx, fail_launches):
                     1 << 22, None)
     msg = L.mxfp8_last_error().decode()
     assert rc == -5 and ("invalid argument" in msg or "tensor map" in msg), msg
+    rc = L.mm_mxfp8_quantized(0x100000, 0x600000, 256, 256, 0x200000, 0x300000, 256,
+                              0x400000, None)
+    msg = L.mxfp8_last_error().decode()
+    assert rc == -5 and ("invalid argument" in msg or "tensor map" in msg), msg
+
+
+def test_mm_quantized_rejects_before_launch(mx):
+    """Shape and pointer checks of the GEMM-only entry (no GPU needed: each
+    returns before any CUDA call)."""
+    L = mx.library()
+    A, S, W, WS, O = 0x100000, 0x200000, 0x300000, 0x400000, 0x500000
+    for M, K, N in [(0, 256, 256), (256, 0, 256), (256, 48, 256), (256, 256, 24),
+                    (-1, 256, 256), (256, 256, 1 << 31)]:
+        assert L.mm_mxfp8_quantized(A, S, M, K, W, WS, N, O, None) == -2, (M, K, N)
+        assert "mm_mxfp8 needs" in L.mxfp8_last_error().decode()
+    for bad in range(5):
+        ptrs = [A, S, W, WS, O]
+        ptrs[bad] = 0 if bad % 2 == 0 else ptrs[bad] + 16
+        assert L.mm_mxfp8_quantized(ptrs[0], ptrs[1], 256, 256, ptrs[2], ptrs[3], 256,
+                                    ptrs[4], None) == -1, bad
+        assert "256-byte aligned" in L.mxfp8_last_error().decode()
 
 
 def test_bounds_checking_build_is_made_and_exports_the_same_calls(mx):

@@ -107,3 +107,42 @@ def test_mm_argument_errors():
     with pytest.raises(mx.MXFP8Error) as e:
         mx.mm_mxfp8(x, wq, ws, workspace=torch.zeros((64,), dtype=torch.uint8, device="cuda"))
     assert e.value.code == -2
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 4096), (200, 272, 1056), (33, 16, 32)])
+def test_norm_quant_feeds_gemm(M, N, K):
+    """rmsnorm_quant_mxfp8 with tiled scales, then mm_mxfp8_quantized on its
+    rowwise plane: the activation codes match the oracle's quantize of the
+    normed bf16 byte for byte, the product is within the bound against the
+    oracle's float64 product of the two quantized operands, and it equals
+    (byte for byte) mm_mxfp8 of the normed bf16, which quantizes it again."""
+    t = W.random_fused(M, K, seed=M + 3 * K, scale=2.0).tensors[0]
+    w = W.random_weights([(N, K)], seed=N + 5 * K).tensors[0].x
+    wq = mx.quantize_weight_for_mm(to_dev(w))
+    nq = mx.rmsnorm_quant_mxfp8(to_dev(t.x), to_dev(t.gamma), t.eps, t.offset, True, False,
+                                scale_layout="mma")
+    out = mx.mm_mxfp8_quantized(nq.q_row, nq.s_row, wq.q_row, wq.s_row)
+    again = mx.mm_mxfp8(nq.normed, wq.q_row, wq.s_row)
+    sync()
+    assert mx.device_status() == 0
+    normed = nq.normed.view(torch.int16).cpu().numpy().view(np.uint16)
+    qx, sx, _, _ = oracle.quant_mxfp8(normed, True, False)
+    assert np.array_equal(nq.q_row.cpu().numpy(), qx)
+    qw, sw, _, _ = oracle.quant_mxfp8(w, True, False)
+    A, B = oracle.dequantize_rowwise(qx, sx), oracle.dequantize_rowwise(qw, sw)
+    ref = A @ B.T
+    got = out.double().cpu().numpy()
+    bound = 2.0**-8 * np.abs(ref) + 2.0**-16 * (np.abs(A) @ np.abs(B).T) + 1e-30
+    assert np.all(np.abs(got - ref) <= bound), float(np.max(np.abs(got - ref) / bound))
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+
+
+def test_mm_quantized_argument_errors():
+    xq = torch.zeros((64, 64), dtype=torch.uint8, device="cuda")
+    wq = torch.zeros((24, 64), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((4096,), dtype=torch.uint8, device="cuda")
+    with pytest.raises(mx.MXFP8Error) as e:
+        mx.mm_mxfp8_quantized(xq, s, wq, s)
+    assert e.value.code == -2
+    with pytest.raises(ValueError):
+        mx.mm_mxfp8_quantized(xq, s, torch.zeros((16, 32), dtype=torch.uint8, device="cuda"), s)
