@@ -14,16 +14,16 @@ struct GemmParams {
     CUtensorMap tma_b;     // B codes [N, K] (K-major), boxes 128 B x 128 rows
     CUtensorMap tma_sfa;   // A scales (tiled layout) as 32-bit words [M/128][K/128][128]
     CUtensorMap tma_sfb;   // B scales, same view; boxes of two 128-row tiles
-    uint16_t* out;         // bf16 [M, N], row-major
+    CUtensorMap tma_out;   // bf16 output [M, N] (row-major), boxes 32 x 32, 64-byte swizzle
     int32_t M, N, K;
     int32_t m_tiles, n_tiles, k_tiles;  // 256-row, 256-column and 128-byte tiles
     int32_t num_tiles;                  // m_tiles * n_tiles output tiles (one per CTA pair)
 };
 
 // Fills p for out[M, N] = A [M, K] x B [N, K]^T (E4M3 codes with tiled UE8M0
-// scales). Returns 0, or -1 / -2 when a tensor map of A / B (codes or scales)
-// cannot be made (a driver without cuTensorMapEncodeTiled, or an address or
-// stride TMA rejects).
+// scales). Returns 0, or -1 / -2 / -3 when a tensor map of A / B (codes or
+// scales) / the output cannot be made (a driver without cuTensorMapEncodeTiled,
+// or an address or stride TMA rejects).
 int gemm_prepare(GemmParams* p, const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                  const uint8_t* sfb, uint16_t* out, int64_t M, int64_t N, int64_t K);
 

@@ -70,7 +70,7 @@ namespace {
 constexpr int kBM = 128;   // A rows per CTA (256 per pair)
 constexpr int kBN = 256;   // output columns per tile; B rows per CTA: kBN / 2
 constexpr int kBK = 128;   // bytes = E4M3 elements per K step
-constexpr int kStages = 6;
+constexpr int kStages = 5;
 constexpr int kThreads = 384;
 constexpr int kEpilogueWarp0 = 4;
 constexpr uint32_t kTileA = kBM * kBK;        // 16 KB
@@ -80,7 +80,11 @@ constexpr uint32_t kSfStage = 3 * kSfTile;    // A tile, then the two B tiles
 constexpr uint32_t kStageTx = kTileA + kTileB + kSfStage;  // bytes one CTA loads per stage
 constexpr uint32_t kOffB = kStages * kTileA;
 constexpr uint32_t kOffSf = kOffB + kStages * kTileB;
-constexpr uint32_t kOffBar = kOffSf + kStages * kSfStage;
+// epilogue staging: per epilogue warp two buffers of one 32-row x 32-column
+// bf16 chunk (64 bytes a row, 64-byte swizzle), the source of its TMA stores
+constexpr uint32_t kEpiBuf = 32 * 64;
+constexpr uint32_t kOffEpi = (kOffSf + kStages * kSfStage + 1023) / 1024 * 1024;
+constexpr uint32_t kOffBar = kOffEpi + 8 * 2 * kEpiBuf;
 constexpr uint32_t kBarBytes = 256;
 constexpr uint32_t kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
 static_assert(8 * (2 * kStages + 3) + 8 <= kBarBytes, "barriers, tensor-memory slot, abort flag");
@@ -214,6 +218,39 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
+}
+
+// TMA store of a 2-D box from this CTA's shared memory, in the thread's
+// bulk async-group; the tensor map clips the parts of the box outside the
+// tensor.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
+                                             int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Until all of this thread's bulk groups have completed (writes performed).
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+// Orders this thread's shared-memory writes before later TMA reads of them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -480,6 +517,8 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
         const int quarter = warp & 3;                   // TMEM lanes 32q .. 32q+31
         const int half = (warp - kEpilogueWarp0) >> 2;  // accumulator columns 128h ..
         const uint32_t lead_tmem_empty = peer_addr(tmem_empty, 0);
+        const uint32_t epi_buf0 = sbase + kOffEpi + (uint32_t)(warp - kEpilogueWarp0) * 2 * kEpiBuf;
+        uint32_t stores = 0;  // TMA stores this warp issued; they alternate between its buffers
         uint32_t local = 0;
         for (int tile = pair; tile < p.num_tiles; tile += pairs, ++local) {
             int m_pair, n_blk;
@@ -501,18 +540,41 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
             tc_fence_before();
             __syncwarp();
             if (lane == 0) bar_arrive_cluster(lead_tmem_empty);
-            const int64_t row = (int64_t)(2 * m_pair + (int)rank) * kBM + 32 * quarter + lane;
+            // store: per 32-column chunk, the warp's 32 rows go to a staging
+            // buffer (row `lane`: 64 bytes, 16-byte piece q at q ^ ((lane >> 1) & 3),
+            // the 64-byte swizzle of the tensor map) and one lane issues a TMA
+            // store of the 32 x 32 box; full lines reach L2, and the stores
+            // run while the warp waits for the next tile
+            // (coordinates compared in 64 bits: inside the tensor they fit in 32)
+            const int64_t row0 = (int64_t)(2 * m_pair + (int)rank) * kBM + 32 * quarter;
             const int64_t col0 = (int64_t)n_blk * kBN + 128 * half;
-            if (row < p.M) {
-                uint16_t* o = p.out + row * p.N + col0;
+            if (row0 < p.M) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (col0 + 8 * j < p.N)
-                        *reinterpret_cast<uint4*>(o + 8 * j) =
-                            make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
-                                       packed[4 * j + 3]);
+                for (int c = 0; c < 4; ++c) {
+                    if (col0 + 32 * c >= p.N) break;
+                    const uint32_t buf = epi_buf0 + (stores & 1u) * kEpiBuf;
+                    // the store that last read this buffer (the one before the
+                    // most recent) is done reading it
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        st_shared_v4(buf + 64u * lane + ((q ^ ((lane >> 1) & 3)) << 4),
+                                     packed[16 * c + 4 * q], packed[16 * c + 4 * q + 1],
+                                     packed[16 * c + 4 * q + 2], packed[16 * c + 4 * q + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&p.tma_out, buf, (int32_t)(col0 + 32 * c), (int32_t)row0);
+                        bulk_commit();
+                    }
+                    ++stores;
+                }
             }
         }
+        // the output is written before the CTA exits
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     // both CTAs done with the pair's barriers and tensor memory
@@ -584,6 +646,21 @@ int encode_scales(CUtensorMap* map, const void* base, int64_t rows, int64_t k_ti
     return r == CUDA_SUCCESS ? 0 : (int)r;
 }
 
+// Tensor map of the bf16 output [M, N] (row-major): boxes of 32 columns x 32
+// rows, 64-byte swizzle (the staging layout of the epilogue).
+int encode_output(CUtensorMap* map, void* base, int64_t M, int64_t N) {
+    EncodeTiled fn = encoder();
+    if (fn == nullptr) return -1;
+    const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)N * 2};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t elem[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, elem,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : (int)r;
+}
+
 constexpr int kMaxDevices = 64;
 
 }  // namespace
@@ -595,7 +672,7 @@ int gemm_prepare(GemmParams* p, const uint8_t* a, const uint8_t* sfa, const uint
         return -1;
     if (encode_operand(&p->tma_b, b, N, K) != 0 || encode_scales(&p->tma_sfb, sfb, N, k_tiles, 2))
         return -2;
-    p->out = out;
+    if (encode_output(&p->tma_out, out, M, N) != 0) return -3;
     p->M = (int32_t)M;
     p->N = (int32_t)N;
     p->K = (int32_t)K;

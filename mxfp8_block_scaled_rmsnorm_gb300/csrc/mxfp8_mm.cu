@@ -56,7 +56,7 @@ int mm_run(const void* x, int64_t M, int64_t K, const void* w_q, const void* w_s
                                     static_cast<uint16_t*>(out), M, N, K);
     if (mr != 0)
         return mx::set_error(MXFP8_ERR_CUDA, "cannot make the TMA tensor map of %s",
-                             mr == -1 ? "x" : "w_q");
+                             mr == -1 ? "x" : mr == -2 ? "w_q" : "out");
     mx::Table<mx::kSmallTable> t;
     std::memset(&t, 0, sizeof t);
     t.n = 1;
@@ -174,7 +174,7 @@ int mm_mxfp8_quantized(const void* x_q, const void* x_s, int64_t M, int64_t K, c
                                     static_cast<uint16_t*>(out), M, N, K);
     if (mr != 0)
         return mx::set_error(MXFP8_ERR_CUDA, "cannot make the TMA tensor map of %s",
-                             mr == -1 ? "x_q" : "w_q");
+                             mr == -1 ? "x_q" : mr == -2 ? "w_q" : "out");
     const int err = mx::launch_gemm(gp, stream);
     return err != cudaSuccess ? gemm_error(err) : MXFP8_OK;
 }
