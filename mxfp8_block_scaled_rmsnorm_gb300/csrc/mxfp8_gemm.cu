@@ -26,7 +26,7 @@
 //  - warp 0 of each CTA: producer. Per K step it loads its A and B
 //    halves (TMA, 128-byte swizzle) and the scale tiles (TMA over a 3-D view
 //    of the tiled scales: its own A tile, both 128-row B tiles, since its
-//    accumulator rows span all 256 columns) into a 6-stage ring. All copies
+//    accumulator rows span all 256 columns) into a 5-stage ring. All copies
 //    of both CTAs complete on the leader CTA's "full" barrier.
 //  - warp 1 of the leader CTA: MMA issuer. Per K step it copies the stage's
 //    scale tiles of both CTAs into their tensor memory (tcgen05.cp
@@ -44,8 +44,13 @@
 //  - warps 4-11: epilogue. Each reads its 32 accumulator lanes (its TMEM lane
 //    quarter, warp % 4) over 128 columns with tcgen05.ld, converts to bf16
 //    (round to nearest even), releases the accumulator (an arrival on the
-//    leader's "tmem_empty"), then stores, so the next tile's MMAs overlap the
-//    stores.
+//    leader's "tmem_empty"), then stores: per 32-column chunk its 32 rows go
+//    to a shared-memory staging buffer (64-byte swizzle, two per warp) and
+//    one lane issues a TMA store of the 32 x 32 box, clipped at the matrix
+//    edges. Whole lines reach L2, and the stores overlap the next tile's
+//    MMAs; stores by each lane of its own row, 16 bytes at a time, had
+//    delayed the next tile's first operand loads and the release behind
+//    them by thousands of cycles per tile.
 //  - Every mbarrier wait gives up after a time limit: it records the site in a
 //    device status word (read by mxfp8_device_status), raises a CTA-wide abort
 //    flag that ends the CTA's other waits, the leader waits (bounded) for the
