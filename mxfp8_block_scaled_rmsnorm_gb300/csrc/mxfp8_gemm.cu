@@ -26,7 +26,7 @@
 //  - warp 0 of each CTA: producer. Per K step it loads its A and B
 //    halves (TMA, 128-byte swizzle) and the scale tiles (TMA over a 3-D view
 //    of the tiled scales: its own A tile, both 128-row B tiles, since its
-//    accumulator rows span all 256 columns) into a 5-stage ring. All copies
+//    accumulator rows span all 256 columns) into a 6-stage ring. All copies
 //    of both CTAs complete on the leader CTA's "full" barrier.
 //  - warp 1 of the leader CTA: MMA issuer. Per K step it copies the stage's
 //    scale tiles of both CTAs into their tensor memory (tcgen05.cp
@@ -45,7 +45,7 @@
 //    quarter, warp % 4) over 128 columns with tcgen05.ld, converts to bf16
 //    (round to nearest even), releases the accumulator (an arrival on the
 //    leader's "tmem_empty"), then stores: per 32-column chunk its 32 rows go
-//    to a shared-memory staging buffer (64-byte swizzle, two per warp) and
+//    to a shared-memory staging buffer (64-byte swizzle, one per warp) and
 //    one lane issues a TMA store of the 32 x 32 box, clipped at the matrix
 //    edges. Whole lines reach L2, and the stores overlap the next tile's
 //    MMAs; stores by each lane of its own row, 16 bytes at a time, had
@@ -75,7 +75,7 @@ namespace {
 constexpr int kBM = 128;   // A rows per CTA (256 per pair)
 constexpr int kBN = 256;   // output columns per tile; B rows per CTA: kBN / 2
 constexpr int kBK = 128;   // bytes = E4M3 elements per K step
-constexpr int kStages = 5;
+constexpr int kStages = 6;
 constexpr int kThreads = 384;
 constexpr int kEpilogueWarp0 = 4;
 constexpr uint32_t kTileA = kBM * kBK;        // 16 KB
@@ -85,11 +85,13 @@ constexpr uint32_t kSfStage = 3 * kSfTile;    // A tile, then the two B tiles
 constexpr uint32_t kStageTx = kTileA + kTileB + kSfStage;  // bytes one CTA loads per stage
 constexpr uint32_t kOffB = kStages * kTileA;
 constexpr uint32_t kOffSf = kOffB + kStages * kTileB;
-// epilogue staging: per epilogue warp two buffers of one 32-row x 32-column
+// epilogue staging: per epilogue warp one buffer of one 32-row x 32-column
 // bf16 chunk (64 bytes a row, 64-byte swizzle), the source of its TMA stores
+// (one buffer, not two, so that the ring has a sixth stage: the ring refills
+// after each tile switch, and five stages left the MMAs waiting there)
 constexpr uint32_t kEpiBuf = 32 * 64;
 constexpr uint32_t kOffEpi = (kOffSf + kStages * kSfStage + 1023) / 1024 * 1024;
-constexpr uint32_t kOffBar = kOffEpi + 8 * 2 * kEpiBuf;
+constexpr uint32_t kOffBar = kOffEpi + 8 * kEpiBuf;
 constexpr uint32_t kBarBytes = 256;
 constexpr uint32_t kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
 static_assert(8 * (2 * kStages + 3) + 8 <= kBarBytes, "barriers, tensor-memory slot, abort flag");
@@ -522,8 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
         const int quarter = warp & 3;                   // TMEM lanes 32q .. 32q+31
         const int half = (warp - kEpilogueWarp0) >> 2;  // accumulator columns 128h ..
         const uint32_t lead_tmem_empty = peer_addr(tmem_empty, 0);
-        const uint32_t epi_buf0 = sbase + kOffEpi + (uint32_t)(warp - kEpilogueWarp0) * 2 * kEpiBuf;
-        uint32_t stores = 0;  // TMA stores this warp issued; they alternate between its buffers
+        const uint32_t buf = sbase + kOffEpi + (uint32_t)(warp - kEpilogueWarp0) * kEpiBuf;
         uint32_t local = 0;
         for (int tile = pair; tile < p.num_tiles; tile += pairs, ++local) {
             int m_pair, n_blk;
@@ -545,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
             tc_fence_before();
             __syncwarp();
             if (lane == 0) bar_arrive_cluster(lead_tmem_empty);
-            // store: per 32-column chunk, the warp's 32 rows go to a staging
+            // store: per 32-column chunk, the warp's 32 rows go to its staging
             // buffer (row `lane`: 64 bytes, 16-byte piece q at q ^ ((lane >> 1) & 3),
             // the 64-byte swizzle of the tensor map) and one lane issues a TMA
             // store of the 32 x 32 box; full lines reach L2, and the stores
@@ -557,10 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     if (col0 + 32 * c >= p.N) break;
-                    const uint32_t buf = epi_buf0 + (stores & 1u) * kEpiBuf;
-                    // the store that last read this buffer (the one before the
-                    // most recent) is done reading it
-                    if (lane == 0) bulk_wait_read<1>();
+                    // the previous store has finished reading the buffer
+                    if (lane == 0) bulk_wait_read<0>();
                     __syncwarp();
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
@@ -573,7 +572,6 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
                         tma_store_2d(&p.tma_out, buf, (int32_t)(col0 + 32 * c), (int32_t)row0);
                         bulk_commit();
                     }
-                    ++stores;
                 }
             }
         }
