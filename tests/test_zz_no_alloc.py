@@ -93,3 +93,32 @@ def test_static_rejects_problems_beyond_its_scratch(lib):
     out = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
     rc, msg = _static(lib, x, wq, out)
     assert rc == -2 and "static scratch" in msg
+
+
+def _act_bytes(M, K):
+    """Scratch the static entry needs: the quantized activation (codes, then
+    tiled scales), each part rounded up to 256 bytes (include/mxfp8norm.h)."""
+    a256 = lambda v: (v + 255) // 256 * 256
+    return a256(M * K) + a256((M + 127) // 128 * 128 * ((K // 32 + 3) // 4) * 4)
+
+
+def test_static_runs_just_under_and_rejects_just_over_its_scratch(lib):
+    """A problem whose activation fills the array to within 32 KB runs and
+    gives the same bytes as mm_mxfp8 (the GEMM takes no scratch of its own);
+    the next size up is refused with MXFP8_ERR_SHAPE, not a CUDA error."""
+    K, N = 4096, 16
+    assert _act_bytes(7936, K) <= SCRATCH_BYTES < _act_bytes(8000, K)
+    assert SCRATCH_BYTES - _act_bytes(7936, K) <= 32 << 10
+    w_bits = W.random_weights([(N, K)], seed=5).tensors[0].x
+    wq = mx.quantize_weight_for_mm(to_dev(w_bits))
+    x = to_dev(W.random_fused(7936, K, seed=6, scale=2.0).tensors[0].x)
+    out_s = torch.full((7936, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    rc, msg = _static(lib, x, wq, out_s)
+    assert rc == 0, msg
+    out_w = mx.mm_mxfp8(x, wq.q_row, wq.s_row)
+    torch.cuda.synchronize()
+    assert torch.equal(out_s.view(torch.int16), out_w.view(torch.int16))
+    x = torch.zeros((8000, K), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((8000, N), dtype=torch.bfloat16, device="cuda")
+    rc, msg = _static(lib, x, wq, out)
+    assert rc == -2 and "static scratch" in msg, msg
