@@ -146,3 +146,24 @@ def test_mm_quantized_argument_errors():
     assert e.value.code == -2
     with pytest.raises(ValueError):
         mx.mm_mxfp8_quantized(xq, s, torch.zeros((16, 32), dtype=torch.uint8, device="cuda"), s)
+
+
+def test_mm_is_deterministic_across_calls_and_streams():
+    """The GEMM accumulates every output in a fixed order (K steps in turn,
+    four 32-element blocks each, one tensor-memory accumulator per tile), so
+    repeated calls give the same bytes, on the default stream and on a side
+    stream alike."""
+    M, N, K = 1000, 2064, 4000
+    x = to_dev(W.random_fused(M, K, seed=11, scale=2.0).tensors[0].x)
+    wq = mx.quantize_weight_for_mm(to_dev(W.random_weights([(N, K)], seed=12).tensors[0].x))
+    first = mx.mm_mxfp8(x, wq.q_row, wq.s_row)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        again = mx.mm_mxfp8(x, wq.q_row, wq.s_row, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    third = mx.mm_mxfp8(x, wq.q_row, wq.s_row)
+    sync()
+    assert mx.device_status() == 0
+    assert torch.equal(first.view(torch.int16), again.view(torch.int16))
+    assert torch.equal(first.view(torch.int16), third.view(torch.int16))
