@@ -222,10 +222,19 @@ def _on_device(dev: torch.device):
     return torch.cuda.device(dev)
 
 
+# torch's current-stream lookup as a raw cudaStream_t: about 0.1 us, against
+# about 3 us for torch.cuda.current_stream().cuda_stream, which builds a
+# Stream object (a large share of a small call's host time)
+_raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_handle(stream, dev) -> int:
     """cudaStream_t of ``stream`` (a torch stream or a raw handle), or of the
     current torch stream on ``dev`` (which must be the current device)."""
     if stream is None:
+        if _raw_current_stream is not None:
+            return _raw_current_stream(torch.cuda.current_device() if dev.index is None
+                                       else dev.index)
         return torch.cuda.current_stream().cuda_stream
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
