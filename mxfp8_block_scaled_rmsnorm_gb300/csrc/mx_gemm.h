@@ -9,6 +9,7 @@
 
 namespace mx {
 
+// The general form: 256 x 256 output tiles per CTA pair.
 struct GemmParams {
     CUtensorMap tma_a;     // A codes [M, K] (K-major), boxes 128 B x 128 rows, 128-byte swizzle
     CUtensorMap tma_b;     // B codes [N, K] (K-major), boxes 128 B x 128 rows
@@ -20,17 +21,43 @@ struct GemmParams {
     int32_t num_tiles;                  // m_tiles * n_tiles output tiles (one per CTA pair)
 };
 
-// Fills p for out[M, N] = A [M, K] x B [N, K]^T (E4M3 codes with tiled UE8M0
-// scales). Returns 0, or -1 / -2 / -3 when a tensor map of A / B (codes or
-// scales) / the output cannot be made (a driver without cuTensorMapEncodeTiled,
-// or an address or stride TMA rejects).
-int gemm_prepare(GemmParams* p, const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
-                 const uint8_t* sfb, uint16_t* out, int64_t M, int64_t N, int64_t K);
+// The form for few activation rows (M <= kSkinnyMaxM): the operands swap
+// roles, so that the weight's rows fill the MMA's 256 rows and the activation
+// rows are its N (32 or 64); the K steps of a 256-column output block are
+// split over the CTA pairs of one cluster, whose float32 partial sums meet in
+// distributed shared memory.
+constexpr int64_t kSkinnyMaxM = 64;
+struct SkinnyParams {
+    CUtensorMap tma_w;     // B codes [N, K] (the weight), boxes 128 B x 128 rows
+    CUtensorMap tma_x;     // A codes [M, K] (the activation), boxes 128 B x mt/2 rows
+    CUtensorMap tma_sfw;   // B scales as 32-bit words [N/128][K/128][128], boxes of one tile
+    CUtensorMap tma_sfx;   // A scales, same view
+    uint16_t* out;         // bf16 [M, N], row-major
+    int32_t M, N, K;
+    int32_t mt;               // activation rows per MMA (32 or 64, >= M)
+    int32_t n_tiles, k_tiles; // 256-column output blocks; 128-byte K steps
+    int32_t splits;           // CTA pairs per cluster, each taking one K range
+    int32_t steps_per_split;  // K steps per range (the last range may be shorter)
+};
 
-// One persistent launch (CTA pairs in clusters of two, one pair per two SMs,
-// at most one pair per output tile) on `stream`; returns the cudaError_t of
-// the launch.
-int launch_gemm(const GemmParams& p, void* stream);
+struct GemmPlan {
+    bool skinny;
+    GemmParams general;
+    SkinnyParams thin;
+};
+
+// Fills plan for out[M, N] = A [M, K] x B [N, K]^T (E4M3 codes with tiled
+// UE8M0 scales), choosing the form by M. Returns 0, or -1 / -2 / -3 when a
+// tensor map of A / B (codes or scales) / the output cannot be made (a driver
+// without cuTensorMapEncodeTiled, or an address or stride TMA rejects).
+int gemm_plan(GemmPlan* plan, const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
+              const uint8_t* sfb, uint16_t* out, int64_t M, int64_t N, int64_t K);
+
+// One persistent launch of the planned form on `stream` (general: CTA pairs
+// in clusters of two, at most one pair per output tile; skinny: clusters of
+// `splits` pairs, at most one cluster per output block); returns the
+// cudaError_t of the launch.
+int gemm_launch(const GemmPlan& plan, void* stream);
 
 // The GEMM's device status word (0: no wait has given up since it was last
 // cleared), read with a synchronizing copy; cleared when asked.

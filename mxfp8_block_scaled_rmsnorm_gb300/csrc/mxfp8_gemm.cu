@@ -56,6 +56,21 @@
 //    flag that ends the CTA's other waits, the leader waits (bounded) for the
 //    pair's copies and MMAs in flight, and both CTAs meet at a cluster barrier,
 //    free their tensor memory and exit.
+//
+// Skinny form (M <= 64 activation rows, e.g. one decoding step): a 256-row
+// output tile would be mostly empty, so the operands swap roles. The weight's
+// 256-row block fills the MMA's M (128 rows per CTA of the pair) and the
+// activation rows are its N (32 or 64, zero rows past M), so out^T is
+// accumulated: weight row n in tensor-memory lane n, activation row m in
+// column m. The tensor cores have little to do and the kernel streams the
+// weight; what bounds it is the MMA warp's issue rate, so a stage holds two
+// K steps (one wait and one commit per eight MMAs) and the four 32-element
+// blocks of a K step add into four separate accumulators (summed by the
+// epilogue; MMAs into one accumulator wait for each other). With few output
+// blocks the K range is split over the two pairs of a 4-CTA cluster; each CTA
+// of the second pair writes its float32 partial to shared memory and the CTA
+// of the first pair with the same lanes adds it through distributed shared
+// memory before storing bf16.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -100,6 +115,46 @@ constexpr uint32_t kColSfa = kBN;                // 4 columns per stage
 constexpr uint32_t kColSfb = kBN + 4 * kStages;  // 8 columns per stage
 static_assert(kColSfb + 8 * kStages <= kTmemCols, "tensor memory budget");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// The skinny form (few activation rows; see SkinnyParams): 256 threads (warp 0
+// producer, warp 1 MMA issuer of the pair's leader, warp 2 tensor-memory
+// allocator, warps 4-7 epilogue), an 8-stage ring of the weight's 128-row
+// tile, the activation's mt/2 rows and both scale tiles per CTA, and a
+// float32 partial-sum area for the split of K over the cluster's pairs.
+constexpr int kSkThreads = 256;
+constexpr int kSkSub = 2;     // K steps per stage: one wait and one commit per 8 MMAs
+constexpr int kSkStages = 4;
+constexpr int kSkMaxMt = 64;
+constexpr uint32_t kSkTileW = 128 * kBK;                 // 16 KB per K step
+constexpr uint32_t kSkTileX = (kSkMaxMt / 2) * kBK;      // 4 KB slot per K step (mt/2 rows used)
+constexpr uint32_t kSkSf = 2 * 512;                      // per K step: weight tile, activation tile
+constexpr uint32_t kSkStageW = kSkSub * kSkTileW;
+constexpr uint32_t kSkStageX = kSkSub * kSkTileX;
+constexpr uint32_t kSkSfStage = kSkSub * kSkSf;
+constexpr uint32_t kSkOffX = kSkStages * kSkStageW;
+constexpr uint32_t kSkOffSf = kSkOffX + kSkStages * kSkStageX;
+// partial sums: per accumulator lane (128) a row of mt float32 padded by 4,
+// so that a warp's 16-byte accesses to consecutive rows hit distinct banks
+constexpr uint32_t kSkOffP = kSkOffSf + kSkStages * kSkSfStage;
+constexpr uint32_t kSkOffBar = kSkOffP + 128 * (kSkMaxMt + 4) * 4;
+constexpr uint32_t kSkSmemBytes = 1024 + kSkOffBar + kBarBytes;
+constexpr int kSkNumBars = 2 * kSkStages + 5;
+static_assert(8 * kSkNumBars + 8 <= kBarBytes, "barriers, tensor-memory slot, abort flag");
+static_assert(kSkSmemBytes <= 232448, "shared memory budget");
+static_assert(kSkOffX % 1024 == 0 && kSkOffSf % 1024 == 0 && kSkOffP % 1024 == 0,
+              "128-byte-swizzled tiles start on 1024-byte boundaries");
+// Four accumulators, one per 32-element block of a K step (block k adds into
+// accumulator k, at columns kSkMaxMt * k ..): four MMAs into one accumulator
+// wait for each other, and with mt columns each is too short to hide that
+// (a K step took as long as a 256-column one); the epilogue adds the four.
+constexpr int kSkChains = 4;
+constexpr uint32_t kSkTmemCols = 512;
+constexpr uint32_t kSkColSfw = kSkChains * kSkMaxMt;            // 4 columns per K step
+constexpr uint32_t kSkColSfx = kSkColSfw + 4 * kSkSub * kSkStages;  // 4 columns per K step
+static_assert(kSkColSfx + 4 * kSkSub * kSkStages <= kSkTmemCols, "tensor memory budget");
+// K split over at most 2 pairs (clusters of 4 CTAs): 4 pairs in 8-CTA
+// clusters measured slower than 2 on every shape tried
+constexpr int kSkMaxSplits = 2;
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
@@ -314,6 +369,16 @@ __device__ __forceinline__ void tc_load32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
+        : "r"(taddr));
+}
+// 16 consecutive float32 columns of this thread's accumulator lane.
+__device__ __forceinline__ void tc_load16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
 __device__ __forceinline__ void tc_wait_load() {
@@ -591,6 +656,326 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
     }
 }
 
+// ----------------------------------------------------- kernel, skinny form ---
+
+// Four float32 from another CTA's shared memory (shared::cluster address).
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ uint16_t bf16_rn(float v) {
+    uint16_t r;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
+    return r;
+}
+
+// out[M, N] for M <= kSkinnyMaxM. Cluster c takes the 256-column output
+// blocks c, c + clusters, ...; pair j of the cluster (CTA ranks 2j, 2j + 1)
+// accumulates the K steps [j * steps_per_split, ...) of the block: weight
+// rows 128 r .. of the block in CTA r's tensor-memory lanes, activation row m
+// in column m. With one pair the epilogue converts and stores; with more,
+// every CTA writes its float32 partial to shared memory and the CTA of pair 0
+// with the same r adds the pairs' partials through distributed shared memory
+// and stores.
+__global__ void __launch_bounds__(kSkThreads, 1)
+    mxfp8_gemm_skinny_kernel(const __grid_constant__ SkinnyParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSkOffBar);
+    // bars[0, S): full; [S, 2S): empty; 2S: tmem_full; 2S+1: tmem_empty;
+    // 2S+2: part_full (partials of the cluster, in pair 0); 2S+3: part_free;
+    // 2S+4: drain (MMA issuer)
+    const uint32_t bar0 = smem_u32(bars);
+    auto full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+    auto empty = [&](int s) { return bar0 + 8u * (uint32_t)(kSkStages + s); };
+    const uint32_t tmem_full = bar0 + 8u * (2 * kSkStages);
+    const uint32_t tmem_empty = tmem_full + 8u;
+    const uint32_t part_full = tmem_full + 16u;
+    const uint32_t part_free = tmem_full + 24u;
+    const uint32_t drain = tmem_full + 32u;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSkOffBar + 8 * kSkNumBars);
+    volatile uint32_t* abort = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t crank = cluster_rank();
+    const uint32_t r = crank & 1u;      // CTA of the pair
+    const uint32_t pbase = crank & ~1u;  // the pair's leader
+    const bool leader = r == 0;
+    const int split = (int)(crank >> 1);
+    const int csize = 2 * p.splits;
+    const int cluster = (int)blockIdx.x / csize, clusters = (int)gridDim.x / csize;
+    const uint16_t pair_mask = (uint16_t)(3u << pbase);
+    const int k0 = split * p.steps_per_split;
+    const int k1 = k0 + p.steps_per_split < p.k_tiles ? k0 + p.steps_per_split : p.k_tiles;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSkStages; ++s) {
+            bar_init(full(s), 1);  // the leader's producer; bytes from both CTAs
+            bar_init(empty(s), 1);
+        }
+        bar_init(tmem_full, 1);
+        bar_init(tmem_empty, 8);                  // the pair's 8 epilogue warps
+        bar_init(part_full, 4 * (uint32_t)p.splits);  // 4 warps of each pair's CTA r
+        bar_init(part_free, 4);  // the adding CTA's 4 warps (pairs other than 0)
+        bar_init(drain, 1);
+        *abort = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kSkTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t x_rows = (uint32_t)p.mt / 2;  // activation rows per CTA
+
+    if (warp == 0) {
+        // ---------------------------------------------------- producer
+        const uint32_t lead_full0 = peer_addr(full(0), pbase);
+        // both K steps of a stage are loaded (one past the range reads data
+        // that is not multiplied, or zeros past K), so the byte count is fixed
+        const uint32_t stage_tx = kSkSub * (kSkTileW + x_rows * kBK + kSkSf);
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t used = 0, last_par = 0;  // per stage: filled at all; parity of its last fill
+        bool ok = true;
+        for (int tile = cluster; ok && tile < p.n_tiles; tile += clusters) {
+            for (int ks = k0; ks < k1; ks += kSkSub) {
+                if (!wait_bar_warp(empty(s), ph ^ 1u, abort, kSiteEmpty)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = lead_full0 + 8u * (uint32_t)s;
+                if (elect_one()) {
+                    if (leader) bar_expect_tx(full(s), 2 * stage_tx);
+#pragma unroll
+                    for (int j = 0; j < kSkSub; ++j) {
+                        const int kt = ks + j;
+                        const uint32_t sf = sbase + kSkOffSf + s * kSkSfStage + j * kSkSf;
+                        tma_load_2d(sbase + s * kSkStageW + j * kSkTileW, &p.tma_w, kt * kBK,
+                                    tile * 256 + (int)r * 128, fb);
+                        tma_load_2d(sbase + kSkOffX + s * kSkStageX + j * kSkTileX, &p.tma_x,
+                                    kt * kBK, (int)(r * x_rows), fb);
+                        tma_load_3d(sf, &p.tma_sfw, 0, kt, 2 * tile + (int)r, fb);
+                        tma_load_3d(sf + 512, &p.tma_sfx, 0, kt, 0, fb);
+                    }
+                }
+                __syncwarp();
+                used |= 1u << s;
+                last_par = (last_par & ~(1u << s)) | (ph << s);
+                if (++s == kSkStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        if (ok) {
+            // every stage's last release has arrived before the CTA may exit
+            for (int i = 0; i < kSkStages; ++i) {
+                if (!wait_bar_warp(empty(s), ph ^ 1u, abort, kSiteEmpty)) break;
+                if (++s == kSkStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        } else if (leader) {
+            // gave up: the pair's copies already issued land before either CTA exits
+            for (int i = 0; i < kSkStages; ++i)
+                if ((used >> i) & 1u) drain_bar(full(i), (last_par >> i) & 1u);
+        }
+    } else if (warp == 1 && leader) {
+        // ---------------------------------------------------- MMA issuer
+        // (as in the general form: the whole warp runs the loop, one elected
+        // lane issues; per K step two scale copies and four 256 x mt x 32 MMAs)
+        int s = 0;
+        uint32_t ph = 0, local = 0;
+        bool ok = true;
+        const uint64_t dw = umma::kmajor_sw128_desc(sbase);
+        const uint64_t dx = umma::kmajor_sw128_desc(sbase + kSkOffX);
+        const uint32_t w_lo0 = (uint32_t)dw, op_hi = (uint32_t)(dw >> 32);
+        const uint32_t x_lo0 = (uint32_t)dx;
+        const uint32_t idesc0 = umma::idesc_mxf8(256, (uint32_t)p.mt, 0, 0);
+        const int full_steps = p.K / kBK;  // K steps with all four 32-element blocks
+        const uint64_t dsf = umma::scale_tile_desc(sbase + kSkOffSf);
+        const uint32_t sf_lo0 = (uint32_t)dsf, sf_hi = (uint32_t)(dsf >> 32);
+        for (int tile = cluster; ok && tile < p.n_tiles; tile += clusters, ++local) {
+            if (!wait_bar_warp(tmem_empty, (local & 1u) ^ 1u, abort, kSiteTmemEmpty)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int ks = k0; ks < k1; ks += kSkSub) {
+                if (!wait_bar_warp(full(s), ph, abort, kSiteFull)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int j = 0; j < kSkSub; ++j) {
+                        const int kt = ks + j;
+                        if (kt >= k1) break;
+                        const uint32_t w_lo = w_lo0 + (((uint32_t)s * kSkStageW + j * kSkTileW) >> 4);
+                        const uint32_t x_lo = x_lo0 + (((uint32_t)s * kSkStageX + j * kSkTileX) >> 4);
+                        const uint32_t sf_lo = sf_lo0 + (((uint32_t)s * kSkSfStage + j * kSkSf) >> 4);
+                        const uint32_t t_sfw = tmem + kSkColSfw + 4u * (kSkSub * s + j);
+                        const uint32_t t_sfx = tmem + kSkColSfx + 4u * (kSkSub * s + j);
+                        tc_copy_scales(t_sfw, desc64(sf_lo, sf_hi));
+                        tc_copy_scales(t_sfx, desc64(sf_lo + (512 >> 4), sf_hi));
+                        const uint32_t en = kt != k0 ? 1u : 0u;
+                        if (kt < full_steps) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                tc_mma(tmem + (uint32_t)(kSkMaxMt * k),
+                                       desc64(w_lo + 2u * k, op_hi), desc64(x_lo + 2u * k, op_hi),
+                                       idesc0 | ((uint32_t)k << 29) | ((uint32_t)k << 4), t_sfw,
+                                       t_sfx, en);
+                        } else {
+                            // the last, partial K step: only the 32-element blocks that exist
+                            const int nk = (p.K - kt * kBK) / 32;
+                            for (int k = 0; k < nk; ++k)
+                                tc_mma(tmem + (uint32_t)(kSkMaxMt * k),
+                                       desc64(w_lo + 2u * k, op_hi), desc64(x_lo + 2u * k, op_hi),
+                                       idesc0 | ((uint32_t)k << 29) | ((uint32_t)k << 4), t_sfw,
+                                       t_sfx, en);
+                        }
+                    }
+                    tc_commit(empty(s), pair_mask);
+                }
+                __syncwarp();
+                if (++s == kSkStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (elect_one()) tc_commit(tmem_full, pair_mask);
+            __syncwarp();
+        }
+        if (!ok) {
+            // gave up: let the pair's scale copies and MMAs finish first
+            if (elect_one()) tc_commit(drain, 1);
+            __syncwarp();
+            drain_bar(drain, 0);
+        }
+    } else if (warp >= 4) {
+        // ---------------------------------------------------- epilogue
+        const int q = warp & 3;  // tensor-memory lanes 32q .. 32q + 31
+        const uint32_t lead_tmem_empty = peer_addr(tmem_empty, pbase);
+        const uint32_t adder_part_full = peer_addr(part_full, r);  // pair 0's CTA r
+        const bool adder = split == 0;
+        const uint32_t pstride = (uint32_t)p.mt + 4u;  // floats per partial row
+        float* my_row = reinterpret_cast<float*>(smem + kSkOffP) + (32 * q + lane) * pstride;
+        const uint32_t my_row_addr = smem_u32(my_row);
+        const int ncol = p.mt / 16;
+        // accumulators that received an MMA: all four, unless this pair's
+        // whole K range is one partial step
+        const int kend = k1 * kBK < p.K ? k1 * kBK : p.K;
+        const int blocks = (kend - k0 * kBK) / 32;
+        const int chains = blocks < kSkChains ? blocks : kSkChains;
+        uint32_t local = 0;
+        for (int tile = cluster; tile < p.n_tiles; tile += clusters, ++local) {
+            const bool ok = wait_bar(tmem_full, local & 1u, abort, kSiteTmemFull);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            tc_fence_after();
+            float acc[kSkMaxMt];
+#pragma unroll
+            for (int m = 0; m < kSkMaxMt; ++m) acc[m] = 0.f;
+            for (int k = 0; k < chains; ++k) {
+#pragma unroll
+                for (int c = 0; c < kSkMaxMt / 16; ++c) {
+                    if (c < ncol) {
+                        uint32_t v[16];
+                        tc_load16(umma::tmem_addr(tmem, 32u * q, kSkMaxMt * k + 16u * c), v);
+                        tc_wait_load();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[16 * c + j] += __uint_as_float(v[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) bar_arrive_cluster(lead_tmem_empty);
+            // this lane's output column (the weight row of its accumulator lane)
+            const int64_t n = (int64_t)tile * 256 + 128 * (int)r + 32 * q + lane;
+            if (p.splits == 1) {
+                if (n < p.N) {
+#pragma unroll
+                    for (int m = 0; m < kSkMaxMt; ++m)
+                        if (m < p.M) p.out[(int64_t)m * p.N + n] = bf16_rn(acc[m]);
+                }
+                continue;
+            }
+            if (!adder) {
+                // the adding CTA has read this CTA's previous partial
+                const bool free_ok =
+                    wait_bar(part_free, (local & 1u) ^ 1u, abort, kSiteTmemEmpty);
+                if (!__all_sync(0xFFFFFFFFu, free_ok)) break;
+#pragma unroll
+                for (int m = 0; m < kSkMaxMt; m += 4)
+                    if (m < p.mt)
+                        *reinterpret_cast<float4*>(my_row + m) =
+                            make_float4(acc[m], acc[m + 1], acc[m + 2], acc[m + 3]);
+            }
+            // every lane's writes ordered before the arrival that publishes them
+            asm volatile("fence.acq_rel.cluster;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) bar_arrive_cluster(adder_part_full);
+            if (!adder) continue;
+            // the adder: its own partial is in registers; the other pairs' rows
+            // are read one pair at a time, all of a row's loads in flight at once
+            const bool full_ok = wait_bar(part_full, local & 1u, abort, kSiteTmemFull);
+            if (!__all_sync(0xFFFFFFFFu, full_ok)) break;
+            for (int j = 1; j < p.splits; ++j) {
+                const uint32_t row = peer_addr(my_row_addr, 2u * (uint32_t)j + r);
+                float4 v[kSkMaxMt / 4];
+#pragma unroll
+                for (int c = 0; c < kSkMaxMt / 4; ++c)
+                    if (4 * c < p.mt) v[c] = ld_cluster_f32x4(row + 16u * c);
+#pragma unroll
+                for (int c = 0; c < kSkMaxMt / 4; ++c) {
+                    if (4 * c < p.mt) {
+                        acc[4 * c] += v[c].x;
+                        acc[4 * c + 1] += v[c].y;
+                        acc[4 * c + 2] += v[c].z;
+                        acc[4 * c + 3] += v[c].w;
+                    }
+                }
+            }
+            if (n < p.N) {
+#pragma unroll
+                for (int m = 0; m < kSkMaxMt; ++m)
+                    if (m < p.M) p.out[(int64_t)m * p.N + n] = bf16_rn(acc[m]);
+            }
+            __syncwarp();
+            // the partials are read: their CTAs may overwrite them
+            if (lane == 0)
+                for (int j = 1; j < p.splits; ++j)
+                    bar_arrive_cluster(peer_addr(part_free, 2u * (uint32_t)j + r));
+        }
+    }
+
+    // every CTA of the cluster done with the barriers, the partials and tensor memory
+    tc_fence_before();
+    cluster_sync();
+    if (warp == 2) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kSkTmemCols)
+                     : "memory");
+    }
+}
+
 // ------------------------------------------------------------------- host ---
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -616,12 +1001,13 @@ EncodeTiled encoder() {
 
 // Tensor map of a K-major E4M3 operand [rows, K]: boxes of 128 bytes of K by
 // 128 rows, 128-byte swizzle, zero fill outside the matrix.
-int encode_operand(CUtensorMap* map, const void* base, int64_t rows, int64_t K) {
+int encode_operand(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                   uint32_t box_rows = 128) {
     EncodeTiled fn = encoder();
     if (fn == nullptr) return -1;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)K};
-    const cuuint32_t box[2] = {(cuuint32_t)kBK, 128};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
     const cuuint32_t elem[2] = {1, 1};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                           strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -666,10 +1052,8 @@ int encode_output(CUtensorMap* map, void* base, int64_t M, int64_t N) {
 
 constexpr int kMaxDevices = 64;
 
-}  // namespace
-
-int gemm_prepare(GemmParams* p, const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
-                 const uint8_t* sfb, uint16_t* out, int64_t M, int64_t N, int64_t K) {
+int prepare_general(GemmParams* p, const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
+                    const uint8_t* sfb, uint16_t* out, int64_t M, int64_t N, int64_t K) {
     const int64_t k_tiles = (K + kBK - 1) / kBK;
     if (encode_operand(&p->tma_a, a, M, K) != 0 || encode_scales(&p->tma_sfa, sfa, M, k_tiles, 1))
         return -1;
@@ -686,8 +1070,108 @@ int gemm_prepare(GemmParams* p, const uint8_t* a, const uint8_t* sfa, const uint
     return 0;
 }
 
-int launch_gemm(const GemmParams& p, void* stream) {
-    if (const int e = hook_launch_error()) return e;
+// SMs of the current device (cached per device), or 0 when it cannot be read.
+int device_sms() {
+    static int cache[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (cache[dev] == 0 &&
+        cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        cache[dev] = 0;
+    }
+    return cache[dev];
+}
+
+// Launch configuration of the skinny form with clusters of 2 * splits CTAs.
+cudaLaunchConfig_t skinny_config(int splits, cudaLaunchAttribute* attr, void* stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kSkThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSkSmemBytes;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    attr->id = cudaLaunchAttributeClusterDimension;
+    attr->val.clusterDim.x = (unsigned)(2 * splits);
+    attr->val.clusterDim.y = 1;
+    attr->val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+// Clusters of 2 * splits CTAs of the skinny form the current device holds at
+// once (cached per device and split count), or 0 when that cannot be read.
+int skinny_resident(int splits) {
+    static int cache[kMaxDevices][kSkMaxSplits + 1] = {};
+    static bool sized[kMaxDevices] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || splits < 1 ||
+        splits > kSkMaxSplits) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (cache[dev][splits] > 0) return cache[dev][splits];
+    if (!sized[dev]) {
+        if (cudaFuncSetAttribute(mxfp8_gemm_skinny_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSkSmemBytes) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        sized[dev] = true;
+    }
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t cfg = skinny_config(splits, &attr, nullptr);
+    const int csize = 2 * splits;
+    cfg.gridDim = dim3((unsigned)(device_sms() / csize * csize), 1, 1);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, mxfp8_gemm_skinny_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cache[dev][splits] = clusters;
+    return clusters;
+}
+
+int prepare_skinny(SkinnyParams* p, const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
+                   const uint8_t* sfb, uint16_t* out, int64_t M, int64_t N, int64_t K) {
+    const int64_t k_tiles = (K + kBK - 1) / kBK;
+    const int mt = M <= 32 ? 32 : 64;
+    if (encode_operand(&p->tma_x, a, M, K, (uint32_t)mt / 2) != 0 ||
+        encode_scales(&p->tma_sfx, sfa, M, k_tiles, 1))
+        return -1;
+    if (encode_operand(&p->tma_w, b, N, K) != 0 || encode_scales(&p->tma_sfw, sfb, N, k_tiles, 1))
+        return -2;
+    p->out = out;
+    p->M = (int32_t)M;
+    p->N = (int32_t)N;
+    p->K = (int32_t)K;
+    p->mt = mt;
+    p->n_tiles = (int32_t)((N + 255) / 256);
+    p->k_tiles = (int32_t)k_tiles;
+    // the K split: the fewest waves of output blocks times K steps per pair
+    // (ties to fewer pairs), every range non-empty
+    int best = 1;
+    int64_t best_cost = -1;
+    for (int splits = 1; splits <= kSkMaxSplits && splits <= k_tiles; ++splits) {
+        const int resident = skinny_resident(splits);
+        if (resident < 1) break;
+        const int64_t waves = (p->n_tiles + resident - 1) / resident;
+        const int64_t cost = waves * ((k_tiles + splits - 1) / splits);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = splits;
+        }
+    }
+    const int64_t per = (k_tiles + best - 1) / best;
+    p->steps_per_split = (int32_t)per;
+    p->splits = (int32_t)((k_tiles + per - 1) / per);
+    return 0;
+}
+
+int launch_general(const GemmParams& p, void* stream) {
     // pairs the device holds at once (the persistent grid: a pair that had to
     // wait for another to finish would run its whole share of tiles late)
     static int resident[kMaxDevices] = {0};
@@ -724,6 +1208,35 @@ int launch_gemm(const GemmParams& p, void* stream) {
     if (pairs <= 0) return cudaSuccess;
     cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
     return (int)cudaLaunchKernelEx(&cfg, mxfp8_gemm_kernel, p);
+}
+
+int launch_skinny(const SkinnyParams& p, void* stream) {
+    if (p.splits < 1 || p.splits > kSkMaxSplits) return (int)cudaErrorInvalidConfiguration;
+    const int resident = skinny_resident(p.splits);
+    if (resident < 1) {
+        const int err = (int)cudaGetLastError();
+        return err != cudaSuccess ? err : (int)cudaErrorInvalidConfiguration;
+    }
+    const int clusters = p.n_tiles < resident ? p.n_tiles : resident;
+    if (clusters <= 0) return cudaSuccess;
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t cfg = skinny_config(p.splits, &attr, stream);
+    cfg.gridDim = dim3((unsigned)(clusters * 2 * p.splits), 1, 1);
+    return (int)cudaLaunchKernelEx(&cfg, mxfp8_gemm_skinny_kernel, p);
+}
+
+}  // namespace
+
+int gemm_plan(GemmPlan* plan, const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
+              const uint8_t* sfb, uint16_t* out, int64_t M, int64_t N, int64_t K) {
+    plan->skinny = M <= kSkinnyMaxM;
+    return plan->skinny ? prepare_skinny(&plan->thin, a, sfa, b, sfb, out, M, N, K)
+                        : prepare_general(&plan->general, a, sfa, b, sfb, out, M, N, K);
+}
+
+int gemm_launch(const GemmPlan& plan, void* stream) {
+    if (const int e = hook_launch_error()) return e;
+    return plan.skinny ? launch_skinny(plan.thin, stream) : launch_general(plan.general, stream);
 }
 
 int gemm_status(bool clear, unsigned long long* out) {

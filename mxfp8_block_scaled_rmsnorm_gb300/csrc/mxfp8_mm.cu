@@ -49,11 +49,11 @@ int mm_run(const void* x, int64_t M, int64_t K, const void* w_q, const void* w_s
     // only the 32-column blocks that exist.
     uint8_t* xq = scratch;
     uint8_t* xs = xq + align256(M * K);
-    mx::GemmParams gp;
-    std::memset(&gp, 0, sizeof gp);
-    const int mr = mx::gemm_prepare(&gp, xq, xs, static_cast<const uint8_t*>(w_q),
-                                    static_cast<const uint8_t*>(w_s),
-                                    static_cast<uint16_t*>(out), M, N, K);
+    mx::GemmPlan plan;
+    std::memset(&plan, 0, sizeof plan);
+    const int mr = mx::gemm_plan(&plan, xq, xs, static_cast<const uint8_t*>(w_q),
+                                 static_cast<const uint8_t*>(w_s), static_cast<uint16_t*>(out),
+                                 M, N, K);
     if (mr != 0)
         return mx::set_error(MXFP8_ERR_CUDA, "cannot make the TMA tensor map of %s",
                              mr == -1 ? "x" : mr == -2 ? "w_q" : "out");
@@ -77,7 +77,7 @@ int mm_run(const void* x, int64_t M, int64_t K, const void* w_q, const void* w_s
                              cudaGetErrorString(static_cast<cudaError_t>(err)));
     }
     // 2. out = x_q w_q^T on the tensor cores
-    err = mx::launch_gemm(gp, stream);
+    err = mx::gemm_launch(plan, stream);
     return err != cudaSuccess ? gemm_error(err) : MXFP8_OK;
 }
 
@@ -165,17 +165,16 @@ int mm_mxfp8_quantized(const void* x_q, const void* x_s, int64_t M, int64_t K, c
     if (rc != MXFP8_OK) return rc;
     if (x_s == nullptr || (reinterpret_cast<uintptr_t>(x_s) & 255u) != 0)
         return mx::set_error(MXFP8_ERR_POINTER, "x_s must be non-NULL and 256-byte aligned");
-    mx::GemmParams gp;
-    std::memset(&gp, 0, sizeof gp);
-    const int mr = mx::gemm_prepare(&gp, static_cast<const uint8_t*>(x_q),
-                                    static_cast<const uint8_t*>(x_s),
-                                    static_cast<const uint8_t*>(w_q),
-                                    static_cast<const uint8_t*>(w_s),
-                                    static_cast<uint16_t*>(out), M, N, K);
+    mx::GemmPlan plan;
+    std::memset(&plan, 0, sizeof plan);
+    const int mr = mx::gemm_plan(&plan, static_cast<const uint8_t*>(x_q),
+                                 static_cast<const uint8_t*>(x_s), static_cast<const uint8_t*>(w_q),
+                                 static_cast<const uint8_t*>(w_s), static_cast<uint16_t*>(out), M,
+                                 N, K);
     if (mr != 0)
         return mx::set_error(MXFP8_ERR_CUDA, "cannot make the TMA tensor map of %s",
                              mr == -1 ? "x_q" : mr == -2 ? "w_q" : "out");
-    const int err = mx::launch_gemm(gp, stream);
+    const int err = mx::gemm_launch(plan, stream);
     return err != cudaSuccess ? gemm_error(err) : MXFP8_OK;
 }
 

@@ -38,7 +38,14 @@ def _abs_bound(x, w):
                                    (33, 256, 7168), (1024, 4096, 4096),
                                    # ragged in all three: partial 256-row and
                                    # 256-column tiles, K % 128 == 32, many pairs
-                                   (1000, 2064, 4000), (200, 272, 1056)])
+                                   (1000, 2064, 4000), (200, 272, 1056),
+                                   # M <= 64 (the swapped-operand form): MMA
+                                   # widths 32 and 64, K split over two pairs
+                                   # (few output blocks) or not, partial last
+                                   # K steps, and the first M of the general form
+                                   (16, 4096, 4096), (48, 2048, 14336), (64, 1040, 896),
+                                   (5, 16, 32), (17, 272, 1056), (32, 14336, 640),
+                                   (64, 512, 640), (65, 512, 1024)])
 def test_mm_matches_oracle(M, N, K):
     x = W.random_fused(M, K, seed=M + K, scale=2.0).tensors[0].x
     w = W.random_weights([(N, K)], seed=N + K).tensors[0].x
@@ -148,12 +155,12 @@ def test_mm_quantized_argument_errors():
         mx.mm_mxfp8_quantized(xq, s, torch.zeros((16, 32), dtype=torch.uint8, device="cuda"), s)
 
 
-def test_mm_is_deterministic_across_calls_and_streams():
+@pytest.mark.parametrize("M,N,K", [(1000, 2064, 4000), (16, 4096, 4096)])
+def test_mm_is_deterministic_across_calls_and_streams(M, N, K):
     """The GEMM accumulates every output in a fixed order (K steps in turn,
-    four 32-element blocks each, one tensor-memory accumulator per tile), so
-    repeated calls give the same bytes, on the default stream and on a side
-    stream alike."""
-    M, N, K = 1000, 2064, 4000
+    four 32-element blocks each; with M <= 64, four accumulators and the K
+    split's partial sums added in pair order), so repeated calls give the same
+    bytes, on the default stream and on a side stream alike."""
     x = to_dev(W.random_fused(M, K, seed=11, scale=2.0).tensors[0].x)
     wq = mx.quantize_weight_for_mm(to_dev(W.random_weights([(N, K)], seed=12).tensors[0].x))
     first = mx.mm_mxfp8(x, wq.q_row, wq.s_row)
