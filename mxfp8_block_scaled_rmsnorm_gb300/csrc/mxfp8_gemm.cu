@@ -462,6 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
         uint32_t ph = 0;
         uint32_t used = 0, last_par = 0;  // per stage: filled at all; parity of its last fill
         bool ok = true;
+        // launched as a programmatic dependent of the previous kernel on the
+        // stream (which may have written A, B or their scales): nothing is
+        // read before it has completed; the set-up above overlapped its tail
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         for (int tile = pair; ok && tile < p.num_tiles; tile += pairs) {
             int m_pair, n_blk;
             tile_coords(p, tile, m_pair, n_blk);
@@ -749,6 +753,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         uint32_t ph = 0;
         uint32_t used = 0, last_par = 0;  // per stage: filled at all; parity of its last fill
         bool ok = true;
+        // launched as a programmatic dependent of the previous kernel on the
+        // stream (which may have written A, B or their scales): nothing is
+        // read before it has completed; the set-up above overlapped its tail
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         for (int tile = cluster; ok && tile < p.n_tiles; tile += clusters) {
             for (int ks = k0; ks < k1; ks += kSkSub) {
                 if (!wait_bar_warp(empty(s), ph ^ 1u, abort, kSiteEmpty)) {
@@ -1183,13 +1191,16 @@ int launch_general(const GemmParams& p, void* stream) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attrs[1];
+    cudaLaunchAttribute attrs[2];
     attrs[0].id = cudaLaunchAttributeClusterDimension;
     attrs[0].val.clusterDim.x = 2;
     attrs[0].val.clusterDim.y = 1;
     attrs[0].val.clusterDim.z = 1;
+    // programmatic dependent launch: set-up overlaps the previous kernel's tail
+    attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attrs;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (resident[dev] == 0) {
         err = (int)cudaFuncSetAttribute(mxfp8_gemm_kernel,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1219,8 +1230,12 @@ int launch_skinny(const SkinnyParams& p, void* stream) {
     }
     const int clusters = p.n_tiles < resident ? p.n_tiles : resident;
     if (clusters <= 0) return cudaSuccess;
-    cudaLaunchAttribute attr;
-    cudaLaunchConfig_t cfg = skinny_config(p.splits, &attr, stream);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = skinny_config(p.splits, attr, stream);
+    // programmatic dependent launch: set-up overlaps the previous kernel's tail
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
     cfg.gridDim = dim3((unsigned)(clusters * 2 * p.splits), 1, 1);
     return (int)cudaLaunchKernelEx(&cfg, mxfp8_gemm_skinny_kernel, p);
 }

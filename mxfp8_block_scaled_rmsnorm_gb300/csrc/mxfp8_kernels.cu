@@ -601,6 +601,9 @@ __device__ __forceinline__ bool warp_full(bool lane_full) {
 template <int MAXN, bool MMA, bool RES>
 __global__ void __launch_bounds__(FusedGeo::kThreads, 4)
 fused_rmsnorm_quant_kernel(const __grid_constant__ Table<MAXN> T) {
+    // let a dependent launch that opted in (the GEMM after a quantize) start
+    // its set-up now: it reads nothing before this grid has completed
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     using G = FusedGeo;
     constexpr int kChunkCols = G::kChunk;
     constexpr int kR = G::kRows;
@@ -784,6 +787,9 @@ fused_rmsnorm_quant_kernel(const __grid_constant__ Table<MAXN> T) {
 template <int MAXN, bool MMA>
 __global__ void __launch_bounds__(QuantGeo::kThreads, 4)
 quant_kernel(const __grid_constant__ Table<MAXN> T) {
+    // let a dependent launch that opted in (the GEMM after a quantize) start
+    // its set-up now: it reads nothing before this grid has completed
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     using G = QuantGeo;
     constexpr int kR = G::kRows;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
