@@ -681,10 +681,10 @@ __device__ __forceinline__ uint16_t bf16_rn(float v) {
 // blocks c, c + clusters, ...; pair j of the cluster (CTA ranks 2j, 2j + 1)
 // accumulates the K steps [j * steps_per_split, ...) of the block: weight
 // rows 128 r .. of the block in CTA r's tensor-memory lanes, activation row m
-// in column m. With one pair the epilogue converts and stores; with more,
-// every CTA writes its float32 partial to shared memory and the CTA of pair 0
-// with the same r adds the pairs' partials through distributed shared memory
-// and stores.
+// in column m (four accumulators, one per 32-element block of a K step). With
+// one pair the epilogue adds the four and stores; with two, the CTAs of pair 1
+// write their float32 sums to shared memory and the CTA of pair 0 with the
+// same r adds them (distributed shared memory) to its own, then stores.
 __global__ void __launch_bounds__(kSkThreads, 1)
     mxfp8_gemm_skinny_kernel(const __grid_constant__ SkinnyParams p) {
     extern __shared__ uint8_t smem_raw[];
