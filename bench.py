@@ -397,8 +397,10 @@ def run_mm(args, world, rank, local, pg):
     timed after 0.4 s of continuous load, when a 1.4 kW part runs at its
     power cap. The roofline is the GEMM kernel alone (mm_mxfp8_quantized on
     the activation quantized once), timed twice: right after a short warm-up
-    ("burst", against 2 x the measured bf16 burst) and after the load
-    (against 2 x the measured sustained bf16)."""
+    ("burst") and after the load. Its bound is the shape's: the tensor cores
+    (against 2 x the measured bf16 burst and sustained figures), or HBM
+    (against the measured copy) where moving the operands once takes longer
+    than the flops at peak, as for decode-sized M."""
     import numpy as np
     import torch
     import mxfp8_block_scaled_rmsnorm_gb300 as mx
@@ -471,6 +473,35 @@ def run_mm(args, world, rank, local, pg):
         src = "measured"
     except Exception:
         bf16, bf16_sus, src = 1900.0, 1700.0, "fallback"
+    hbm, hbm_src = measured_peak()
+    # the GEMM's algorithmic bytes: both operands' codes and scales read once,
+    # the bf16 output written once
+    gemm_bytes = float((N + M) * K + (N + M) * (K // 32) + 2 * M * N)
+    # the roofline that bounds the shape: a decode-sized M leaves the tensor
+    # cores idle behind the weight's stream from HBM
+    if gemm_bytes / (hbm * 1e9) > flops / (2 * bf16 * 1e12):
+        gbs = lambda t: gemm_bytes / (t * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": "mxfp8_gemm_skinny_kernel (mm_mxfp8_quantized)"
+                if M <= 128 else "mxfp8_gemm_kernel (mm_mxfp8_quantized)",
+                "achieved": gbs(gemm_ms), "peak": hbm, "unit": "GB/s",
+                "frac": gbs(gemm_ms) / hbm, "avg_launch_us": gemm_ms * 1e3,
+                "bytes_per_launch": gemm_bytes,
+                "peak_source": f"{hbm_src} hbm_gbs (copy)",
+                "burst": {"achieved": gbs(burst_ms), "frac": gbs(burst_ms) / hbm,
+                          "avg_launch_us": burst_ms * 1e3},
+                "tensor_frac": tf(gemm_ms) / (2 * bf16_sus), "traffic": None}
+    else:
+        roof = {"bound": "tensor", "kernel": "mxfp8_gemm_kernel (mm_mxfp8_quantized)",
+                "achieved": tf(gemm_ms), "peak": 2 * bf16_sus, "unit": "TFLOP/s",
+                "frac": tf(gemm_ms) / (2 * bf16_sus), "avg_launch_us": gemm_ms * 1e3,
+                "peak_source": f"{src} sustained bf16 x 2 (nominal fp8/bf16 ratio): "
+                               "timed after 0.4 s of load",
+                "burst": {"achieved": tf(burst_ms), "peak": 2 * bf16,
+                          "frac": tf(burst_ms) / (2 * bf16),
+                          "avg_launch_us": burst_ms * 1e3,
+                          "peak_source": f"{src} burst bf16 x 2: timed right after "
+                                         "a short warm-up"},
+                "traffic": None}
     if rank == 0:
         print(json.dumps({
             "metric": "TFLOP/s of mm_mxfp8 (on-the-fly activation quantize + block-scaled GEMM)",
@@ -478,26 +509,22 @@ def run_mm(args, world, rank, local, pg):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
             "config": {"workload": f"mm_mxfp8-{M}x{N}x{K}", "M": M, "N": N, "K": K,
-                       "gemm": "mxfp8_gemm_kernel: tcgen05 cta_group::2 kind::mxf8f6f4 "
-                               "block-scaled (E4M3 x E4M3, UE8M0 per 32), 256x256 tiles per "
-                               "CTA pair, float32 accumulation in tensor memory, TMA-store "
-                               "bf16 epilogue",
+                       "gemm": ("mxfp8_gemm_skinny_kernel: tcgen05 cta_group::2 "
+                                "kind::mxf8f6f4 block-scaled (E4M3 x E4M3, UE8M0 per 32), "
+                                "operands swapped (the weight's 256-row block is the MMA's M, "
+                                "the activation rows its N), K split over the CTA pairs of a "
+                                "cluster when output blocks are few"
+                                if M <= 128 else
+                                "mxfp8_gemm_kernel: tcgen05 cta_group::2 kind::mxf8f6f4 "
+                                "block-scaled (E4M3 x E4M3, UE8M0 per 32), 256x256 tiles per "
+                                "CTA pair, float32 accumulation in tensor memory, TMA-store "
+                                "bf16 epilogue"),
                        "l2": ("operands fit in L2 (%.0f MB): a 256 MB memset and a 256 MB "
                               "read flush L2 before every timed launch, outside its events"
                               % (in_bytes / 1e6)
                               if flush is not None else
                               "operands larger than L2 (%.0f MB); no flush" % (in_bytes / 1e6))},
-            "roofline": {"bound": "tensor", "kernel": "mxfp8_gemm_kernel (mm_mxfp8_quantized)",
-                         "achieved": tf(gemm_ms), "peak": 2 * bf16_sus, "unit": "TFLOP/s",
-                         "frac": tf(gemm_ms) / (2 * bf16_sus), "avg_launch_us": gemm_ms * 1e3,
-                         "peak_source": f"{src} sustained bf16 x 2 (nominal fp8/bf16 ratio): "
-                                        "timed after 0.4 s of load",
-                         "burst": {"achieved": tf(burst_ms), "peak": 2 * bf16,
-                                   "frac": tf(burst_ms) / (2 * bf16),
-                                   "avg_launch_us": burst_ms * 1e3,
-                                   "peak_source": f"{src} burst bf16 x 2: timed right after "
-                                                  "a short warm-up"},
-                         "traffic": None},
+            "roofline": roof,
             "clocks": clk, "gpu_launches": 2 * args.steps}), flush=True)
     return 0
 

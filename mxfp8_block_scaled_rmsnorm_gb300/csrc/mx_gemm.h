@@ -23,18 +23,18 @@ struct GemmParams {
 
 // The form for few activation rows (M <= kSkinnyMaxM): the operands swap
 // roles, so that the weight's rows fill the MMA's 256 rows and the activation
-// rows are its N (32 or 64); the K steps of a 256-column output block are
+// rows are its N (32, 64 or 128); the K steps of a 256-column output block are
 // split over the CTA pairs of one cluster, whose float32 partial sums meet in
 // distributed shared memory.
-constexpr int64_t kSkinnyMaxM = 64;
+constexpr int64_t kSkinnyMaxM = 128;
 struct SkinnyParams {
     CUtensorMap tma_w;     // B codes [N, K] (the weight), boxes 128 B x 128 rows
     CUtensorMap tma_x;     // A codes [M, K] (the activation), boxes 128 B x mt/2 rows
     CUtensorMap tma_sfw;   // B scales as 32-bit words [N/128][K/128][128], boxes of one tile
     CUtensorMap tma_sfx;   // A scales, same view
-    uint16_t* out;         // bf16 [M, N], row-major
+    CUtensorMap tma_out;   // bf16 output [M, N] (row-major), boxes 32 columns x mt rows
     int32_t M, N, K;
-    int32_t mt;               // activation rows per MMA (32 or 64, >= M)
+    int32_t mt;               // activation rows per MMA (32, 64 or 128, >= M)
     int32_t n_tiles, k_tiles; // 256-column output blocks; 128-byte K steps
     int32_t splits;           // CTA pairs per cluster, each taking one K range
     int32_t steps_per_split;  // K steps per range (the last range may be shorter)

@@ -57,16 +57,17 @@
 //    pair's copies and MMAs in flight, and both CTAs meet at a cluster barrier,
 //    free their tensor memory and exit.
 //
-// Skinny form (M <= 64 activation rows, e.g. one decoding step): a 256-row
-// output tile would be mostly empty, so the operands swap roles. The weight's
-// 256-row block fills the MMA's M (128 rows per CTA of the pair) and the
-// activation rows are its N (32 or 64, zero rows past M), so out^T is
-// accumulated: weight row n in tensor-memory lane n, activation row m in
-// column m. The tensor cores have little to do and the kernel streams the
-// weight; what bounds it is the MMA warp's issue rate, so a stage holds two
-// K steps (one wait and one commit per eight MMAs) and the four 32-element
-// blocks of a K step add into four separate accumulators (summed by the
-// epilogue; MMAs into one accumulator wait for each other). With few output
+// Skinny form (M <= 128 activation rows, e.g. decoding steps): a 256-row
+// output tile would be mostly empty, and few tiles would leave most SMs idle,
+// so the operands swap roles. The weight's 256-row block fills the MMA's M
+// (128 rows per CTA of the pair) and the activation rows are its N (32, 64
+// or 128, zero rows past M), so out^T is accumulated: weight row n in
+// tensor-memory lane n, activation row m in column m. The tensor cores have
+// little to do and the kernel streams the weight; what bounds it is the MMA
+// warp's issue rate, so a stage holds two K steps (one wait and one commit
+// per eight MMAs) and the four 32-element blocks of a K step add into four
+// separate accumulators (two for N = 128; summed by the epilogue; MMAs into
+// one accumulator wait for each other). With few output
 // blocks the K range is split over the two pairs of a 4-CTA cluster; each CTA
 // of the second pair writes its float32 partial to shared memory and the CTA
 // of the first pair with the same lanes adds it through distributed shared
@@ -118,40 +119,46 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // The skinny form (few activation rows; see SkinnyParams): 256 threads (warp 0
 // producer, warp 1 MMA issuer of the pair's leader, warp 2 tensor-memory
-// allocator, warps 4-7 epilogue), an 8-stage ring of the weight's 128-row
-// tile, the activation's mt/2 rows and both scale tiles per CTA, and a
-// float32 partial-sum area for the split of K over the cluster's pairs.
+// allocator, warps 4-7 epilogue), a ring of stages of two K steps each (the
+// weight's 128-row tile, the activation's mt/2 rows and both scale tiles per
+// CTA and K step), and a float32 partial-sum area for the split of K over the
+// cluster's pairs. Two instances: up to 64 activation rows (mt 32 or 64) and
+// up to 128 (mt 128), whose larger activation tiles and partial rows leave
+// shared memory for three stages instead of four.
 constexpr int kSkThreads = 256;
-constexpr int kSkSub = 2;     // K steps per stage: one wait and one commit per 8 MMAs
-constexpr int kSkStages = 4;
-constexpr int kSkMaxMt = 64;
-constexpr uint32_t kSkTileW = 128 * kBK;                 // 16 KB per K step
-constexpr uint32_t kSkTileX = (kSkMaxMt / 2) * kBK;      // 4 KB slot per K step (mt/2 rows used)
-constexpr uint32_t kSkSf = 2 * 512;                      // per K step: weight tile, activation tile
-constexpr uint32_t kSkStageW = kSkSub * kSkTileW;
-constexpr uint32_t kSkStageX = kSkSub * kSkTileX;
-constexpr uint32_t kSkSfStage = kSkSub * kSkSf;
-constexpr uint32_t kSkOffX = kSkStages * kSkStageW;
-constexpr uint32_t kSkOffSf = kSkOffX + kSkStages * kSkStageX;
-// partial sums: per accumulator lane (128) a row of mt float32 padded by 4,
-// so that a warp's 16-byte accesses to consecutive rows hit distinct banks
-constexpr uint32_t kSkOffP = kSkOffSf + kSkStages * kSkSfStage;
-constexpr uint32_t kSkOffBar = kSkOffP + 128 * (kSkMaxMt + 4) * 4;
-constexpr uint32_t kSkSmemBytes = 1024 + kSkOffBar + kBarBytes;
-constexpr int kSkNumBars = 2 * kSkStages + 5;
-static_assert(8 * kSkNumBars + 8 <= kBarBytes, "barriers, tensor-memory slot, abort flag");
-static_assert(kSkSmemBytes <= 232448, "shared memory budget");
-static_assert(kSkOffX % 1024 == 0 && kSkOffSf % 1024 == 0 && kSkOffP % 1024 == 0,
-              "128-byte-swizzled tiles start on 1024-byte boundaries");
-// Four accumulators, one per 32-element block of a K step (block k adds into
-// accumulator k, at columns kSkMaxMt * k ..): four MMAs into one accumulator
-// wait for each other, and with mt columns each is too short to hide that
-// (a K step took as long as a 256-column one); the epilogue adds the four.
-constexpr int kSkChains = 4;
+constexpr int kSkSub = 2;                 // K steps per stage: one wait and one commit per 8 MMAs
+constexpr uint32_t kSkTileW = 128 * kBK;  // 16 KB per K step
+constexpr uint32_t kSkSf = 2 * 512;       // per K step: weight tile, activation tile
 constexpr uint32_t kSkTmemCols = 512;
-constexpr uint32_t kSkColSfw = kSkChains * kSkMaxMt;            // 4 columns per K step
-constexpr uint32_t kSkColSfx = kSkColSfw + 4 * kSkSub * kSkStages;  // 4 columns per K step
-static_assert(kSkColSfx + 4 * kSkSub * kSkStages <= kSkTmemCols, "tensor memory budget");
+template <int MT>  // the largest mt of the instance: 64 or 128
+struct SkLayout {
+    static constexpr int kStages = MT <= 64 ? 4 : 3;
+    static constexpr uint32_t kTileX = (MT / 2) * kBK;  // slot per K step (mt/2 rows used)
+    static constexpr uint32_t kStageW = kSkSub * kSkTileW;
+    static constexpr uint32_t kStageX = kSkSub * kTileX;
+    static constexpr uint32_t kSfStage = kSkSub * kSkSf;
+    static constexpr uint32_t kOffX = kStages * kStageW;
+    static constexpr uint32_t kOffSf = kOffX + kStages * kStageX;
+    // partial sums: per accumulator lane (128) a row of MT float32 padded by 4,
+    // so that a warp's 16-byte accesses to consecutive rows hit distinct banks
+    static constexpr uint32_t kOffP = kOffSf + kStages * kSfStage;
+    static constexpr uint32_t kOffBar = kOffP + 128 * (MT + 4) * 4;
+    static constexpr uint32_t kSmemBytes = 1024 + kOffBar + kBarBytes;
+    static constexpr int kNumBars = 2 * kStages + 5;
+    // One accumulator per 32-element block of a K step (block k adds into
+    // accumulator k % kChains, at columns MT * (k % kChains) ..): MMAs into one
+    // accumulator wait for each other, and with mt <= 64 columns each is too
+    // short to hide that (a K step took as long as a 256-column one); the
+    // epilogue adds the accumulators. Four of 64 columns, or two of 128.
+    static constexpr int kChains = 256 / MT;
+    static constexpr uint32_t kColSfw = kChains * MT;                  // 4 columns per K step
+    static constexpr uint32_t kColSfx = kColSfw + 4 * kSkSub * kStages;  // 4 columns per K step
+    static_assert(8 * kNumBars + 8 <= kBarBytes, "barriers, tensor-memory slot, abort flag");
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kOffX % 1024 == 0 && kOffSf % 1024 == 0 && kOffP % 1024 == 0,
+                  "128-byte-swizzled tiles start on 1024-byte boundaries");
+    static_assert(kColSfx + 4 * kSkSub * kStages <= kSkTmemCols, "tensor memory budget");
+};
 // K split over at most 2 pairs (clusters of 4 CTAs): 4 pairs in 8-CTA
 // clusters measured slower than 2 on every shape tried
 constexpr int kSkMaxSplits = 2;
@@ -371,14 +378,19 @@ __device__ __forceinline__ void tc_load32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[31])
         : "r"(taddr));
 }
-// 16 consecutive float32 columns of this thread's accumulator lane.
-__device__ __forceinline__ void tc_load16(uint32_t taddr, uint32_t (&r)[16]) {
+// The same into float registers (the load moves 32-bit words).
+__device__ __forceinline__ void tc_load32f(uint32_t taddr, float (&r)[32]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32"
-        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+        " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31},"
+        " [%32];"
+        : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]),
+          "=f"(r[7]), "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]),
+          "=f"(r[13]), "=f"(r[14]), "=f"(r[15]), "=f"(r[16]), "=f"(r[17]), "=f"(r[18]),
+          "=f"(r[19]), "=f"(r[20]), "=f"(r[21]), "=f"(r[22]), "=f"(r[23]), "=f"(r[24]),
+          "=f"(r[25]), "=f"(r[26]), "=f"(r[27]), "=f"(r[28]), "=f"(r[29]), "=f"(r[30]),
+          "=f"(r[31])
         : "r"(taddr));
 }
 __device__ __forceinline__ void tc_wait_load() {
@@ -671,6 +683,9 @@ __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
                  : "memory");
     return v;
 }
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
 __device__ __forceinline__ uint16_t bf16_rn(float v) {
     uint16_t r;
     asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
@@ -681,29 +696,33 @@ __device__ __forceinline__ uint16_t bf16_rn(float v) {
 // blocks c, c + clusters, ...; pair j of the cluster (CTA ranks 2j, 2j + 1)
 // accumulates the K steps [j * steps_per_split, ...) of the block: weight
 // rows 128 r .. of the block in CTA r's tensor-memory lanes, activation row m
-// in column m (four accumulators, one per 32-element block of a K step). With
-// one pair the epilogue adds the four and stores; with two, the CTAs of pair 1
+// in column m of each accumulator (the 32-element blocks of a K step spread
+// over kChains of them). With one pair the epilogue adds the accumulators and
+// stores; with two, the CTAs of pair 1
 // write their float32 sums to shared memory and the CTA of pair 0 with the
 // same r adds them (distributed shared memory) to its own, then stores.
+template <int MT>
 __global__ void __launch_bounds__(kSkThreads, 1)
     mxfp8_gemm_skinny_kernel(const __grid_constant__ SkinnyParams p) {
+    using L = SkLayout<MT>;
+    constexpr int kStages = L::kStages, kChains = L::kChains;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSkOffBar);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
     // bars[0, S): full; [S, 2S): empty; 2S: tmem_full; 2S+1: tmem_empty;
     // 2S+2: part_full (partials of the cluster, in pair 0); 2S+3: part_free;
     // 2S+4: drain (MMA issuer)
     const uint32_t bar0 = smem_u32(bars);
     auto full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
-    auto empty = [&](int s) { return bar0 + 8u * (uint32_t)(kSkStages + s); };
-    const uint32_t tmem_full = bar0 + 8u * (2 * kSkStages);
+    auto empty = [&](int s) { return bar0 + 8u * (uint32_t)(kStages + s); };
+    const uint32_t tmem_full = bar0 + 8u * (2 * kStages);
     const uint32_t tmem_empty = tmem_full + 8u;
     const uint32_t part_full = tmem_full + 16u;
     const uint32_t part_free = tmem_full + 24u;
     const uint32_t drain = tmem_full + 32u;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSkOffBar + 8 * kSkNumBars);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffBar + 8 * L::kNumBars);
     volatile uint32_t* abort = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -718,7 +737,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     const int k0 = split * p.steps_per_split;
     const int k1 = k0 + p.steps_per_split < p.k_tiles ? k0 + p.steps_per_split : p.k_tiles;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kSkStages; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             bar_init(full(s), 1);  // the leader's producer; bytes from both CTAs
             bar_init(empty(s), 1);
         }
@@ -769,10 +788,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 #pragma unroll
                     for (int j = 0; j < kSkSub; ++j) {
                         const int kt = ks + j;
-                        const uint32_t sf = sbase + kSkOffSf + s * kSkSfStage + j * kSkSf;
-                        tma_load_2d(sbase + s * kSkStageW + j * kSkTileW, &p.tma_w, kt * kBK,
+                        const uint32_t sf = sbase + L::kOffSf + s * L::kSfStage + j * kSkSf;
+                        tma_load_2d(sbase + s * L::kStageW + j * kSkTileW, &p.tma_w, kt * kBK,
                                     tile * 256 + (int)r * 128, fb);
-                        tma_load_2d(sbase + kSkOffX + s * kSkStageX + j * kSkTileX, &p.tma_x,
+                        tma_load_2d(sbase + L::kOffX + s * L::kStageX + j * L::kTileX, &p.tma_x,
                                     kt * kBK, (int)(r * x_rows), fb);
                         tma_load_3d(sf, &p.tma_sfw, 0, kt, 2 * tile + (int)r, fb);
                         tma_load_3d(sf + 512, &p.tma_sfx, 0, kt, 0, fb);
@@ -781,7 +800,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 __syncwarp();
                 used |= 1u << s;
                 last_par = (last_par & ~(1u << s)) | (ph << s);
-                if (++s == kSkStages) {
+                if (++s == kStages) {
                     s = 0;
                     ph ^= 1u;
                 }
@@ -789,16 +808,16 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         }
         if (ok) {
             // every stage's last release has arrived before the CTA may exit
-            for (int i = 0; i < kSkStages; ++i) {
+            for (int i = 0; i < kStages; ++i) {
                 if (!wait_bar_warp(empty(s), ph ^ 1u, abort, kSiteEmpty)) break;
-                if (++s == kSkStages) {
+                if (++s == kStages) {
                     s = 0;
                     ph ^= 1u;
                 }
             }
         } else if (leader) {
             // gave up: the pair's copies already issued land before either CTA exits
-            for (int i = 0; i < kSkStages; ++i)
+            for (int i = 0; i < kStages; ++i)
                 if ((used >> i) & 1u) drain_bar(full(i), (last_par >> i) & 1u);
         }
     } else if (warp == 1 && leader) {
@@ -809,12 +828,12 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         uint32_t ph = 0, local = 0;
         bool ok = true;
         const uint64_t dw = umma::kmajor_sw128_desc(sbase);
-        const uint64_t dx = umma::kmajor_sw128_desc(sbase + kSkOffX);
+        const uint64_t dx = umma::kmajor_sw128_desc(sbase + L::kOffX);
         const uint32_t w_lo0 = (uint32_t)dw, op_hi = (uint32_t)(dw >> 32);
         const uint32_t x_lo0 = (uint32_t)dx;
         const uint32_t idesc0 = umma::idesc_mxf8(256, (uint32_t)p.mt, 0, 0);
         const int full_steps = p.K / kBK;  // K steps with all four 32-element blocks
-        const uint64_t dsf = umma::scale_tile_desc(sbase + kSkOffSf);
+        const uint64_t dsf = umma::scale_tile_desc(sbase + L::kOffSf);
         const uint32_t sf_lo0 = (uint32_t)dsf, sf_hi = (uint32_t)(dsf >> 32);
         for (int tile = cluster; ok && tile < p.n_tiles; tile += clusters, ++local) {
             if (!wait_bar_warp(tmem_empty, (local & 1u) ^ 1u, abort, kSiteTmemEmpty)) {
@@ -833,35 +852,37 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     for (int j = 0; j < kSkSub; ++j) {
                         const int kt = ks + j;
                         if (kt >= k1) break;
-                        const uint32_t w_lo = w_lo0 + (((uint32_t)s * kSkStageW + j * kSkTileW) >> 4);
-                        const uint32_t x_lo = x_lo0 + (((uint32_t)s * kSkStageX + j * kSkTileX) >> 4);
-                        const uint32_t sf_lo = sf_lo0 + (((uint32_t)s * kSkSfStage + j * kSkSf) >> 4);
-                        const uint32_t t_sfw = tmem + kSkColSfw + 4u * (kSkSub * s + j);
-                        const uint32_t t_sfx = tmem + kSkColSfx + 4u * (kSkSub * s + j);
+                        const uint32_t w_lo = w_lo0 + (((uint32_t)s * L::kStageW + j * kSkTileW) >> 4);
+                        const uint32_t x_lo = x_lo0 + (((uint32_t)s * L::kStageX + j * L::kTileX) >> 4);
+                        const uint32_t sf_lo = sf_lo0 + (((uint32_t)s * L::kSfStage + j * kSkSf) >> 4);
+                        const uint32_t t_sfw = tmem + L::kColSfw + 4u * (kSkSub * s + j);
+                        const uint32_t t_sfx = tmem + L::kColSfx + 4u * (kSkSub * s + j);
                         tc_copy_scales(t_sfw, desc64(sf_lo, sf_hi));
                         tc_copy_scales(t_sfx, desc64(sf_lo + (512 >> 4), sf_hi));
+                        // block k of the range's first K step starts its
+                        // accumulator; every later block adds into it
                         const uint32_t en = kt != k0 ? 1u : 0u;
                         if (kt < full_steps) {
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
-                                tc_mma(tmem + (uint32_t)(kSkMaxMt * k),
+                                tc_mma(tmem + (uint32_t)(MT * (k % kChains)),
                                        desc64(w_lo + 2u * k, op_hi), desc64(x_lo + 2u * k, op_hi),
                                        idesc0 | ((uint32_t)k << 29) | ((uint32_t)k << 4), t_sfw,
-                                       t_sfx, en);
+                                       t_sfx, k >= kChains ? 1u : en);
                         } else {
                             // the last, partial K step: only the 32-element blocks that exist
                             const int nk = (p.K - kt * kBK) / 32;
                             for (int k = 0; k < nk; ++k)
-                                tc_mma(tmem + (uint32_t)(kSkMaxMt * k),
+                                tc_mma(tmem + (uint32_t)(MT * (k % kChains)),
                                        desc64(w_lo + 2u * k, op_hi), desc64(x_lo + 2u * k, op_hi),
                                        idesc0 | ((uint32_t)k << 29) | ((uint32_t)k << 4), t_sfw,
-                                       t_sfx, en);
+                                       t_sfx, k >= kChains ? 1u : en);
                         }
                     }
                     tc_commit(empty(s), pair_mask);
                 }
                 __syncwarp();
-                if (++s == kSkStages) {
+                if (++s == kStages) {
                     s = 0;
                     ph ^= 1u;
                 }
@@ -883,94 +904,112 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         const uint32_t adder_part_full = peer_addr(part_full, r);  // pair 0's CTA r
         const bool adder = split == 0;
         const uint32_t pstride = (uint32_t)p.mt + 4u;  // floats per partial row
-        float* my_row = reinterpret_cast<float*>(smem + kSkOffP) + (32 * q + lane) * pstride;
+        float* my_row = reinterpret_cast<float*>(smem + L::kOffP) + (32 * q + lane) * pstride;
         const uint32_t my_row_addr = smem_u32(my_row);
-        const int ncol = p.mt / 16;
-        // accumulators that received an MMA: all four, unless this pair's
+        // accumulators that received an MMA: all of them, unless this pair's
         // whole K range is one partial step
         const int kend = k1 * kBK < p.K ? k1 * kBK : p.K;
         const int blocks = (kend - k0 * kBK) / 32;
-        const int chains = blocks < kSkChains ? blocks : kSkChains;
+        const int chains = blocks < kChains ? blocks : kChains;
+        // the warp's bf16 staging buffer for its TMA store (row m of the
+        // 32-column box at 64 m bytes), in this CTA's own partial-sum area,
+        // which only CTAs that never store write partials into
+        const uint32_t stage = smem_u32(smem + L::kOffP) + (uint32_t)q * (MT * 64u);
         uint32_t local = 0;
         for (int tile = cluster; tile < p.n_tiles; tile += clusters, ++local) {
             const bool ok = wait_bar(tmem_full, local & 1u, abort, kSiteTmemFull);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             tc_fence_after();
-            float acc[kSkMaxMt];
+            // accumulator 0 straight into acc (all its loads in flight), the
+            // others added 32 columns at a time (columns past mt are not read)
+            float acc[MT];
 #pragma unroll
-            for (int m = 0; m < kSkMaxMt; ++m) acc[m] = 0.f;
-            for (int k = 0; k < chains; ++k) {
+            for (int c = 0; c < MT / 32; ++c)
+                if (32 * c < p.mt)
+                    tc_load32f(umma::tmem_addr(tmem, 32u * q, 32u * c),
+                               *reinterpret_cast<float(*)[32]>(&acc[32 * c]));
+            tc_wait_load();
+            for (int k = 1; k < chains; ++k) {
 #pragma unroll
-                for (int c = 0; c < kSkMaxMt / 16; ++c) {
-                    if (c < ncol) {
-                        uint32_t v[16];
-                        tc_load16(umma::tmem_addr(tmem, 32u * q, kSkMaxMt * k + 16u * c), v);
+                for (int c = 0; c < MT / 32; ++c) {
+                    if (32 * c < p.mt) {
+                        uint32_t v[32];
+                        tc_load32(umma::tmem_addr(tmem, 32u * q, MT * k + 32u * c), v);
                         tc_wait_load();
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) acc[16 * c + j] += __uint_as_float(v[j]);
+                        for (int j = 0; j < 32; ++j) acc[32 * c + j] += __uint_as_float(v[j]);
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) bar_arrive_cluster(lead_tmem_empty);
-            // this lane's output column (the weight row of its accumulator lane)
-            const int64_t n = (int64_t)tile * 256 + 128 * (int)r + 32 * q + lane;
-            if (p.splits == 1) {
-                if (n < p.N) {
+            if (p.splits > 1) {
+                if (!adder) {
+                    // the adding CTA has read this CTA's previous partial
+                    const bool free_ok =
+                        wait_bar(part_free, (local & 1u) ^ 1u, abort, kSiteTmemEmpty);
+                    if (!__all_sync(0xFFFFFFFFu, free_ok)) break;
 #pragma unroll
-                    for (int m = 0; m < kSkMaxMt; ++m)
-                        if (m < p.M) p.out[(int64_t)m * p.N + n] = bf16_rn(acc[m]);
+                    for (int m = 0; m < MT; m += 4)
+                        if (m < p.mt)
+                            *reinterpret_cast<float4*>(my_row + m) =
+                                make_float4(acc[m], acc[m + 1], acc[m + 2], acc[m + 3]);
                 }
-                continue;
-            }
-            if (!adder) {
-                // the adding CTA has read this CTA's previous partial
-                const bool free_ok =
-                    wait_bar(part_free, (local & 1u) ^ 1u, abort, kSiteTmemEmpty);
-                if (!__all_sync(0xFFFFFFFFu, free_ok)) break;
+                // every lane's writes ordered before the arrival that publishes them
+                asm volatile("fence.acq_rel.cluster;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) bar_arrive_cluster(adder_part_full);
+                if (!adder) continue;
+                // the adder: its own partial is in registers; the other pairs'
+                // rows are read one pair at a time, 64 floats in flight at once
+                const bool full_ok = wait_bar(part_full, local & 1u, abort, kSiteTmemFull);
+                if (!__all_sync(0xFFFFFFFFu, full_ok)) break;
+                constexpr int kGroup = 16;  // float4 loads in flight
+                for (int j = 1; j < p.splits; ++j) {
+                    const uint32_t row = peer_addr(my_row_addr, 2u * (uint32_t)j + r);
 #pragma unroll
-                for (int m = 0; m < kSkMaxMt; m += 4)
-                    if (m < p.mt)
-                        *reinterpret_cast<float4*>(my_row + m) =
-                            make_float4(acc[m], acc[m + 1], acc[m + 2], acc[m + 3]);
-            }
-            // every lane's writes ordered before the arrival that publishes them
-            asm volatile("fence.acq_rel.cluster;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) bar_arrive_cluster(adder_part_full);
-            if (!adder) continue;
-            // the adder: its own partial is in registers; the other pairs' rows
-            // are read one pair at a time, all of a row's loads in flight at once
-            const bool full_ok = wait_bar(part_full, local & 1u, abort, kSiteTmemFull);
-            if (!__all_sync(0xFFFFFFFFu, full_ok)) break;
-            for (int j = 1; j < p.splits; ++j) {
-                const uint32_t row = peer_addr(my_row_addr, 2u * (uint32_t)j + r);
-                float4 v[kSkMaxMt / 4];
+                    for (int c0 = 0; c0 < MT / 4; c0 += kGroup) {
+                        float4 v[kGroup];
 #pragma unroll
-                for (int c = 0; c < kSkMaxMt / 4; ++c)
-                    if (4 * c < p.mt) v[c] = ld_cluster_f32x4(row + 16u * c);
+                        for (int c = 0; c < kGroup; ++c)
+                            if (4 * (c0 + c) < p.mt)
+                                v[c] = ld_cluster_f32x4(row + 16u * (c0 + c));
 #pragma unroll
-                for (int c = 0; c < kSkMaxMt / 4; ++c) {
-                    if (4 * c < p.mt) {
-                        acc[4 * c] += v[c].x;
-                        acc[4 * c + 1] += v[c].y;
-                        acc[4 * c + 2] += v[c].z;
-                        acc[4 * c + 3] += v[c].w;
+                        for (int c = 0; c < kGroup; ++c) {
+                            if (4 * (c0 + c) < p.mt) {
+                                acc[4 * (c0 + c)] += v[c].x;
+                                acc[4 * (c0 + c) + 1] += v[c].y;
+                                acc[4 * (c0 + c) + 2] += v[c].z;
+                                acc[4 * (c0 + c) + 3] += v[c].w;
+                            }
+                        }
                     }
                 }
+                __syncwarp();
+                // the partials are read: their CTAs may overwrite them
+                if (lane == 0)
+                    for (int j = 1; j < p.splits; ++j)
+                        bar_arrive_cluster(peer_addr(part_free, 2u * (uint32_t)j + r));
             }
-            if (n < p.N) {
-#pragma unroll
-                for (int m = 0; m < kSkMaxMt; ++m)
-                    if (m < p.M) p.out[(int64_t)m * p.N + n] = bf16_rn(acc[m]);
-            }
+            // the warp's 32 output columns (the weight rows of its accumulator
+            // lanes), all mt rows: bf16 into the staging buffer, then one TMA
+            // store of the box, which the tensor map clips at M and N
+            const int64_t n0 = (int64_t)tile * 256 + 128 * (int)r + 32 * q;
+            if (lane == 0) bulk_wait_read<0>();  // the previous tile's store has read it
             __syncwarp();
-            // the partials are read: their CTAs may overwrite them
-            if (lane == 0)
-                for (int j = 1; j < p.splits; ++j)
-                    bar_arrive_cluster(peer_addr(part_free, 2u * (uint32_t)j + r));
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (m < p.mt) st_shared_u16(stage + 64u * m + 2u * lane, bf16_rn(acc[m]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && n0 < p.N) {
+                tma_store_2d(&p.tma_out, stage, (int32_t)n0, 0);
+                bulk_commit();
+            }
         }
+        // the stores have completed before the CTA exits
+        if (lane == 0) bulk_wait_all();
     }
 
     // every CTA of the cluster done with the barriers, the partials and tensor memory
@@ -1043,17 +1082,19 @@ int encode_scales(CUtensorMap* map, const void* base, int64_t rows, int64_t k_ti
     return r == CUDA_SUCCESS ? 0 : (int)r;
 }
 
-// Tensor map of the bf16 output [M, N] (row-major): boxes of 32 columns x 32
-// rows, 64-byte swizzle (the staging layout of the epilogue).
-int encode_output(CUtensorMap* map, void* base, int64_t M, int64_t N) {
+// Tensor map of the bf16 output [M, N] (row-major): boxes of 32 columns x
+// box_rows rows, the staging layout of the epilogue: 64-byte swizzle (the
+// general form) or none (the skinny form).
+int encode_output(CUtensorMap* map, void* base, int64_t M, int64_t N, uint32_t box_rows = 32,
+                  CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_64B) {
     EncodeTiled fn = encoder();
     if (fn == nullptr) return -1;
     const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
     const cuuint64_t strides[1] = {(cuuint64_t)N * 2};
-    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t box[2] = {32, box_rows};
     const cuuint32_t elem[2] = {1, 1};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, elem,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? 0 : (int)r;
 }
@@ -1094,11 +1135,13 @@ int device_sms() {
     return cache[dev];
 }
 
-// Launch configuration of the skinny form with clusters of 2 * splits CTAs.
+// Launch configuration of the skinny form's instance MT with clusters of
+// 2 * splits CTAs.
+template <int MT>
 cudaLaunchConfig_t skinny_config(int splits, cudaLaunchAttribute* attr, void* stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kSkThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSkSmemBytes;
+    cfg.dynamicSmemBytes = SkLayout<MT>::kSmemBytes;
     cfg.stream = static_cast<cudaStream_t>(stream);
     attr->id = cudaLaunchAttributeClusterDimension;
     attr->val.clusterDim.x = (unsigned)(2 * splits);
@@ -1109,8 +1152,10 @@ cudaLaunchConfig_t skinny_config(int splits, cudaLaunchAttribute* attr, void* st
     return cfg;
 }
 
-// Clusters of 2 * splits CTAs of the skinny form the current device holds at
-// once (cached per device and split count), or 0 when that cannot be read.
+// Clusters of 2 * splits CTAs of the skinny form's instance MT the current
+// device holds at once (cached per device and split count), or 0 when that
+// cannot be read.
+template <int MT>
 int skinny_resident(int splits) {
     static int cache[kMaxDevices][kSkMaxSplits + 1] = {};
     static bool sized[kMaxDevices] = {false};
@@ -1122,20 +1167,21 @@ int skinny_resident(int splits) {
     }
     if (cache[dev][splits] > 0) return cache[dev][splits];
     if (!sized[dev]) {
-        if (cudaFuncSetAttribute(mxfp8_gemm_skinny_kernel,
+        if (cudaFuncSetAttribute(mxfp8_gemm_skinny_kernel<MT>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSkSmemBytes) != cudaSuccess) {
+                                 (int)SkLayout<MT>::kSmemBytes) != cudaSuccess) {
             cudaGetLastError();
             return 0;
         }
         sized[dev] = true;
     }
     cudaLaunchAttribute attr;
-    cudaLaunchConfig_t cfg = skinny_config(splits, &attr, nullptr);
+    cudaLaunchConfig_t cfg = skinny_config<MT>(splits, &attr, nullptr);
     const int csize = 2 * splits;
     cfg.gridDim = dim3((unsigned)(device_sms() / csize * csize), 1, 1);
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, mxfp8_gemm_skinny_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, mxfp8_gemm_skinny_kernel<MT>, &cfg) !=
+        cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -1143,16 +1189,22 @@ int skinny_resident(int splits) {
     return clusters;
 }
 
+// The instance for mt activation rows: 64 for mt <= 64, else 128.
+int skinny_resident(int mt, int splits) {
+    return mt <= 64 ? skinny_resident<64>(splits) : skinny_resident<128>(splits);
+}
+
 int prepare_skinny(SkinnyParams* p, const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
                    const uint8_t* sfb, uint16_t* out, int64_t M, int64_t N, int64_t K) {
     const int64_t k_tiles = (K + kBK - 1) / kBK;
-    const int mt = M <= 32 ? 32 : 64;
+    const int mt = M <= 32 ? 32 : M <= 64 ? 64 : 128;
     if (encode_operand(&p->tma_x, a, M, K, (uint32_t)mt / 2) != 0 ||
         encode_scales(&p->tma_sfx, sfa, M, k_tiles, 1))
         return -1;
     if (encode_operand(&p->tma_w, b, N, K) != 0 || encode_scales(&p->tma_sfw, sfb, N, k_tiles, 1))
         return -2;
-    p->out = out;
+    if (encode_output(&p->tma_out, out, M, N, (uint32_t)mt, CU_TENSOR_MAP_SWIZZLE_NONE) != 0)
+        return -3;
     p->M = (int32_t)M;
     p->N = (int32_t)N;
     p->K = (int32_t)K;
@@ -1164,7 +1216,7 @@ int prepare_skinny(SkinnyParams* p, const uint8_t* a, const uint8_t* sfa, const 
     int best = 1;
     int64_t best_cost = -1;
     for (int splits = 1; splits <= kSkMaxSplits && splits <= k_tiles; ++splits) {
-        const int resident = skinny_resident(splits);
+        const int resident = skinny_resident(mt, splits);
         if (resident < 1) break;
         const int64_t waves = (p->n_tiles + resident - 1) / resident;
         const int64_t cost = waves * ((k_tiles + splits - 1) / splits);
@@ -1221,9 +1273,10 @@ int launch_general(const GemmParams& p, void* stream) {
     return (int)cudaLaunchKernelEx(&cfg, mxfp8_gemm_kernel, p);
 }
 
+template <int MT>
 int launch_skinny(const SkinnyParams& p, void* stream) {
     if (p.splits < 1 || p.splits > kSkMaxSplits) return (int)cudaErrorInvalidConfiguration;
-    const int resident = skinny_resident(p.splits);
+    const int resident = skinny_resident<MT>(p.splits);
     if (resident < 1) {
         const int err = (int)cudaGetLastError();
         return err != cudaSuccess ? err : (int)cudaErrorInvalidConfiguration;
@@ -1231,13 +1284,17 @@ int launch_skinny(const SkinnyParams& p, void* stream) {
     const int clusters = p.n_tiles < resident ? p.n_tiles : resident;
     if (clusters <= 0) return cudaSuccess;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = skinny_config(p.splits, attr, stream);
+    cudaLaunchConfig_t cfg = skinny_config<MT>(p.splits, attr, stream);
     // programmatic dependent launch: set-up overlaps the previous kernel's tail
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.numAttrs = 2;
     cfg.gridDim = dim3((unsigned)(clusters * 2 * p.splits), 1, 1);
-    return (int)cudaLaunchKernelEx(&cfg, mxfp8_gemm_skinny_kernel, p);
+    return (int)cudaLaunchKernelEx(&cfg, mxfp8_gemm_skinny_kernel<MT>, p);
+}
+
+int launch_skinny(const SkinnyParams& p, void* stream) {
+    return p.mt <= 64 ? launch_skinny<64>(p, stream) : launch_skinny<128>(p, stream);
 }
 
 }  // namespace
