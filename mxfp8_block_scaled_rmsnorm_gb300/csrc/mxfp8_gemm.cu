@@ -139,10 +139,12 @@ struct SkLayout {
     static constexpr uint32_t kSfStage = kSkSub * kSkSf;
     static constexpr uint32_t kOffX = kStages * kStageW;
     static constexpr uint32_t kOffSf = kOffX + kStages * kStageX;
-    // partial sums: per accumulator lane (128) a row of MT float32 padded by 4,
-    // so that a warp's 16-byte accesses to consecutive rows hit distinct banks
+    // the adding CTA's receive area for the other pair's partial sums: for
+    // each accumulator lane (128) MT float32, per epilogue warp q a region of
+    // float4 groups [MT / 4][32 lanes] (so a warp's 16-byte accesses cover
+    // 512 contiguous bytes), which then holds the warp's bf16 output staging
     static constexpr uint32_t kOffP = kOffSf + kStages * kSfStage;
-    static constexpr uint32_t kOffBar = kOffP + 128 * (MT + 4) * 4;
+    static constexpr uint32_t kOffBar = kOffP + 128 * MT * 4;
     static constexpr uint32_t kSmemBytes = 1024 + kOffBar + kBarBytes;
     static constexpr int kNumBars = 2 * kStages + 5;
     // One accumulator per 32-element block of a K step (block k adds into
@@ -160,7 +162,8 @@ struct SkLayout {
     static_assert(kColSfx + 4 * kSkSub * kStages <= kSkTmemCols, "tensor memory budget");
 };
 // K split over at most 2 pairs (clusters of 4 CTAs): 4 pairs in 8-CTA
-// clusters measured slower than 2 on every shape tried
+// clusters measured slower than 2 on every shape tried (the exchange of
+// partial sums below has one receive area, for pair 1)
 constexpr int kSkMaxSplits = 2;
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
@@ -674,10 +677,20 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
 
 // ----------------------------------------------------- kernel, skinny form ---
 
-// Four float32 from another CTA's shared memory (shared::cluster address).
-__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
+// Four 32-bit words into another CTA's shared memory (shared::cluster
+// addresses), counted as 16 bytes on that CTA's barrier `bar`.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d, uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
+        "[%5];" ::"r"(addr),
+        "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
+        : "memory");
+}
+// Four float32 from this CTA's shared memory.
+__device__ __forceinline__ float4 ld_shared_f32x4(uint32_t addr) {
     float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                  : "r"(addr)
                  : "memory");
@@ -712,7 +725,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
     // bars[0, S): full; [S, 2S): empty; 2S: tmem_full; 2S+1: tmem_empty;
-    // 2S+2: part_full (partials of the cluster, in pair 0); 2S+3: part_free;
+    // 2S+2: part_full (pair 1's partials received, in pair 0); 2S+3: part_free
+    // (pair 0's receive area free again, in pair 1);
     // 2S+4: drain (MMA issuer)
     const uint32_t bar0 = smem_u32(bars);
     auto full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
@@ -743,8 +757,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         }
         bar_init(tmem_full, 1);
         bar_init(tmem_empty, 8);                  // the pair's 8 epilogue warps
-        bar_init(part_full, 4 * (uint32_t)p.splits);  // 4 warps of each pair's CTA r
-        bar_init(part_free, 4);  // the adding CTA's 4 warps (pairs other than 0)
+        bar_init(part_full, 1);  // the adding CTA's expected bytes; pair 1's partials
+        bar_init(part_free, 4);  // the adding CTA's 4 warps (in pair 1)
         bar_init(drain, 1);
         *abort = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -903,20 +917,24 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         const uint32_t lead_tmem_empty = peer_addr(tmem_empty, pbase);
         const uint32_t adder_part_full = peer_addr(part_full, r);  // pair 0's CTA r
         const bool adder = split == 0;
-        const uint32_t pstride = (uint32_t)p.mt + 4u;  // floats per partial row
-        float* my_row = reinterpret_cast<float*>(smem + L::kOffP) + (32 * q + lane) * pstride;
-        const uint32_t my_row_addr = smem_u32(my_row);
+        // the warp's region of the receive area (in pair 0's CTA r); this
+        // lane's float4 group c at + 512 c
+        const uint32_t region = smem_u32(smem + L::kOffP) + (uint32_t)q * (MT * 128u);
+        const uint32_t my_part = region + 16u * (uint32_t)lane;
+        const uint32_t adder_part = peer_addr(my_part, r);
         // accumulators that received an MMA: all of them, unless this pair's
         // whole K range is one partial step
         const int kend = k1 * kBK < p.K ? k1 * kBK : p.K;
         const int blocks = (kend - k0 * kBK) / 32;
         const int chains = blocks < kChains ? blocks : kChains;
         // the warp's bf16 staging buffer for its TMA store (row m of the
-        // 32-column box at 64 m bytes), in this CTA's own partial-sum area,
-        // which only CTAs that never store write partials into
-        const uint32_t stage = smem_u32(smem + L::kOffP) + (uint32_t)q * (MT * 64u);
+        // 32-column box at 64 m bytes): the start of its region, once read
+        const uint32_t stage = region;
         uint32_t local = 0;
-        for (int tile = cluster; tile < p.n_tiles; tile += clusters, ++local) {
+        bool expected = false;  // pair 0: this tile's receive bytes announced
+        int tile = cluster;
+        for (; tile < p.n_tiles; tile += clusters, ++local) {
+            expected = false;
             const bool ok = wait_bar(tmem_full, local & 1u, abort, kSiteTmemFull);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             tc_fence_after();
@@ -946,51 +964,37 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             if (lane == 0) bar_arrive_cluster(lead_tmem_empty);
             if (p.splits > 1) {
                 if (!adder) {
-                    // the adding CTA has read this CTA's previous partial
+                    // pair 1: once pair 0's CTA r has stored its previous
+                    // tile, the partials go straight into its receive area
                     const bool free_ok =
                         wait_bar(part_free, (local & 1u) ^ 1u, abort, kSiteTmemEmpty);
                     if (!__all_sync(0xFFFFFFFFu, free_ok)) break;
 #pragma unroll
                     for (int m = 0; m < MT; m += 4)
                         if (m < p.mt)
-                            *reinterpret_cast<float4*>(my_row + m) =
-                                make_float4(acc[m], acc[m + 1], acc[m + 2], acc[m + 3]);
+                            st_async_v4(adder_part + 128u * (uint32_t)m, __float_as_uint(acc[m]),
+                                        __float_as_uint(acc[m + 1]), __float_as_uint(acc[m + 2]),
+                                        __float_as_uint(acc[m + 3]), adder_part_full);
+                    continue;
                 }
-                // every lane's writes ordered before the arrival that publishes them
-                asm volatile("fence.acq_rel.cluster;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) bar_arrive_cluster(adder_part_full);
-                if (!adder) continue;
-                // the adder: its own partial is in registers; the other pairs'
-                // rows are read one pair at a time, 64 floats in flight at once
+                // pair 0: all of pair 1's bytes for this tile have landed
+                if (warp == 4 && lane == 0) bar_expect_tx(part_full, 512u * (uint32_t)p.mt);
+                expected = true;
                 const bool full_ok = wait_bar(part_full, local & 1u, abort, kSiteTmemFull);
                 if (!__all_sync(0xFFFFFFFFu, full_ok)) break;
-                constexpr int kGroup = 16;  // float4 loads in flight
-                for (int j = 1; j < p.splits; ++j) {
-                    const uint32_t row = peer_addr(my_row_addr, 2u * (uint32_t)j + r);
+                expected = false;
 #pragma unroll
-                    for (int c0 = 0; c0 < MT / 4; c0 += kGroup) {
-                        float4 v[kGroup];
-#pragma unroll
-                        for (int c = 0; c < kGroup; ++c)
-                            if (4 * (c0 + c) < p.mt)
-                                v[c] = ld_cluster_f32x4(row + 16u * (c0 + c));
-#pragma unroll
-                        for (int c = 0; c < kGroup; ++c) {
-                            if (4 * (c0 + c) < p.mt) {
-                                acc[4 * (c0 + c)] += v[c].x;
-                                acc[4 * (c0 + c) + 1] += v[c].y;
-                                acc[4 * (c0 + c) + 2] += v[c].z;
-                                acc[4 * (c0 + c) + 3] += v[c].w;
-                            }
-                        }
+                for (int m = 0; m < MT; m += 4) {
+                    if (m < p.mt) {
+                        const float4 v = ld_shared_f32x4(my_part + 128u * (uint32_t)m);
+                        acc[m] += v.x;
+                        acc[m + 1] += v.y;
+                        acc[m + 2] += v.z;
+                        acc[m + 3] += v.w;
                     }
                 }
+                // every lane has read the region before any overwrites it
                 __syncwarp();
-                // the partials are read: their CTAs may overwrite them
-                if (lane == 0)
-                    for (int j = 1; j < p.splits; ++j)
-                        bar_arrive_cluster(peer_addr(part_free, 2u * (uint32_t)j + r));
             }
             // the warp's 32 output columns (the weight rows of its accumulator
             // lanes), all mt rows: bf16 into the staging buffer, then one TMA
@@ -1007,6 +1011,18 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 tma_store_2d(&p.tma_out, stage, (int32_t)n0, 0);
                 bulk_commit();
             }
+            if (p.splits > 1 && lane == 0) {
+                // the store has read the staging: pair 1 may send the next tile
+                bulk_wait_read<0>();
+                bar_arrive_cluster(peer_addr(part_free, 2u + r));
+            }
+        }
+        // gave up with pair 1 possibly still sending this tile's partials:
+        // they land (bounded wait) before the CTA may exit
+        if (tile < p.n_tiles && p.splits > 1 && adder && warp == 4) {
+            if (lane == 0 && !expected) bar_expect_tx(part_full, 512u * (uint32_t)p.mt);
+            __syncwarp();
+            drain_bar(part_full, local & 1u);
         }
         // the stores have completed before the CTA exits
         if (lane == 0) bulk_wait_all();
