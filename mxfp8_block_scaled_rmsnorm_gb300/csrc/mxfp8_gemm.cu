@@ -67,11 +67,12 @@
 // warp's issue rate, so a stage holds two K steps (one wait and one commit
 // per eight MMAs) and the four 32-element blocks of a K step add into four
 // separate accumulators (two for N = 128; summed by the epilogue; MMAs into
-// one accumulator wait for each other). With few output
-// blocks the K range is split over the two pairs of a 4-CTA cluster; each CTA
-// of the second pair writes its float32 partial to shared memory and the CTA
-// of the first pair with the same lanes adds it through distributed shared
-// memory before storing bf16.
+// one accumulator wait for each other). With few output blocks the K range is
+// split over two or three pairs of a cluster; in turn, each CTA of a later
+// pair writes its float32 partial straight into the shared memory of the
+// first pair's CTA with the same lanes (st.async, counted on that CTA's
+// mbarrier), which adds it. That CTA then stages its bf16 output in the same
+// shared memory and writes it with TMA stores.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -161,10 +162,11 @@ struct SkLayout {
                   "128-byte-swizzled tiles start on 1024-byte boundaries");
     static_assert(kColSfx + 4 * kSkSub * kStages <= kSkTmemCols, "tensor memory budget");
 };
-// K split over at most 2 pairs (clusters of 4 CTAs): 4 pairs in 8-CTA
-// clusters measured slower than 2 on every shape tried (the exchange of
-// partial sums below has one receive area, for pair 1)
-constexpr int kSkMaxSplits = 2;
+// K split over at most 3 pairs (clusters of up to 6 CTAs); pair 0 receives
+// the other pairs' partial sums in turn. Four pairs in 8-CTA clusters
+// measured slower than three on every shape tried (1.3-2x; fewer such
+// clusters are resident at once).
+constexpr int kSkMaxSplits = 3;
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
@@ -711,9 +713,9 @@ __device__ __forceinline__ uint16_t bf16_rn(float v) {
 // rows 128 r .. of the block in CTA r's tensor-memory lanes, activation row m
 // in column m of each accumulator (the 32-element blocks of a K step spread
 // over kChains of them). With one pair the epilogue adds the accumulators and
-// stores; with two, the CTAs of pair 1
-// write their float32 sums to shared memory and the CTA of pair 0 with the
-// same r adds them (distributed shared memory) to its own, then stores.
+// stores; with more, the CTAs of pairs 1, 2 send their float32 sums in turn
+// into the receive area of pair 0's CTA with the same r, which adds them to
+// its own, then stores.
 template <int MT>
 __global__ void __launch_bounds__(kSkThreads, 1)
     mxfp8_gemm_skinny_kernel(const __grid_constant__ SkinnyParams p) {
@@ -725,8 +727,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
     // bars[0, S): full; [S, 2S): empty; 2S: tmem_full; 2S+1: tmem_empty;
-    // 2S+2: part_full (pair 1's partials received, in pair 0); 2S+3: part_free
-    // (pair 0's receive area free again, in pair 1);
+    // 2S+2: part_full (another pair's partials received, in pair 0);
+    // 2S+3: part_free (pair 0's receive area free for this pair, in pairs >= 1);
     // 2S+4: drain (MMA issuer)
     const uint32_t bar0 = smem_u32(bars);
     auto full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
@@ -757,8 +759,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         }
         bar_init(tmem_full, 1);
         bar_init(tmem_empty, 8);                  // the pair's 8 epilogue warps
-        bar_init(part_full, 1);  // the adding CTA's expected bytes; pair 1's partials
-        bar_init(part_free, 4);  // the adding CTA's 4 warps (in pair 1)
+        bar_init(part_full, 1);  // (pair 0) the expected bytes; one other pair's partials
+        bar_init(part_free, 4);  // (pairs j >= 1) pair 0's CTA r's 4 warps: pair j's turn
         bar_init(drain, 1);
         *abort = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -930,10 +932,15 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         // the warp's bf16 staging buffer for its TMA store (row m of the
         // 32-column box at 64 m bytes): the start of its region, once read
         const uint32_t stage = region;
+        // pair 0 receives the other pairs' partials in turn, one receive
+        // phase each: phase local * (splits - 1) + j - 1 holds pair j's
+        const uint32_t sends = (uint32_t)p.splits - 1u;
         uint32_t local = 0;
-        bool expected = false;  // pair 0: this tile's receive bytes announced
+        uint32_t pending = 0;   // pair 0: the receive phase waited for next
+        bool expected = false;  // pair 0: that phase's bytes announced
         int tile = cluster;
         for (; tile < p.n_tiles; tile += clusters, ++local) {
+            pending = local * sends;
             expected = false;
             const bool ok = wait_bar(tmem_full, local & 1u, abort, kSiteTmemFull);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
@@ -964,10 +971,12 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             if (lane == 0) bar_arrive_cluster(lead_tmem_empty);
             if (p.splits > 1) {
                 if (!adder) {
-                    // pair 1: once pair 0's CTA r has stored its previous
-                    // tile, the partials go straight into its receive area
-                    const bool free_ok =
-                        wait_bar(part_free, (local & 1u) ^ 1u, abort, kSiteTmemEmpty);
+                    // pair j >= 1: its turn has come (pair 1: pair 0's CTA r
+                    // has stored the previous tile; pair j > 1: pair 0 has
+                    // added pair j - 1's partials of this tile), then the
+                    // partials go straight into pair 0's receive area
+                    const uint32_t parity = split == 1 ? (local & 1u) ^ 1u : local & 1u;
+                    const bool free_ok = wait_bar(part_free, parity, abort, kSiteTmemEmpty);
                     if (!__all_sync(0xFFFFFFFFu, free_ok)) break;
 #pragma unroll
                     for (int m = 0; m < MT; m += 4)
@@ -977,24 +986,34 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                                         __float_as_uint(acc[m + 3]), adder_part_full);
                     continue;
                 }
-                // pair 0: all of pair 1's bytes for this tile have landed
-                if (warp == 4 && lane == 0) bar_expect_tx(part_full, 512u * (uint32_t)p.mt);
-                expected = true;
-                const bool full_ok = wait_bar(part_full, local & 1u, abort, kSiteTmemFull);
-                if (!__all_sync(0xFFFFFFFFu, full_ok)) break;
-                expected = false;
-#pragma unroll
-                for (int m = 0; m < MT; m += 4) {
-                    if (m < p.mt) {
-                        const float4 v = ld_shared_f32x4(my_part + 128u * (uint32_t)m);
-                        acc[m] += v.x;
-                        acc[m + 1] += v.y;
-                        acc[m + 2] += v.z;
-                        acc[m + 3] += v.w;
+                bool got = true;
+                for (int j = 1; j < p.splits; ++j) {
+                    // pair 0: all of pair j's bytes for this tile have landed
+                    if (warp == 4 && lane == 0) bar_expect_tx(part_full, 512u * (uint32_t)p.mt);
+                    expected = true;
+                    const bool full_ok = wait_bar(part_full, pending & 1u, abort, kSiteTmemFull);
+                    if (!__all_sync(0xFFFFFFFFu, full_ok)) {
+                        got = false;
+                        break;
                     }
+                    expected = false;
+                    ++pending;
+#pragma unroll
+                    for (int m = 0; m < MT; m += 4) {
+                        if (m < p.mt) {
+                            const float4 v = ld_shared_f32x4(my_part + 128u * (uint32_t)m);
+                            acc[m] += v.x;
+                            acc[m + 1] += v.y;
+                            acc[m + 2] += v.z;
+                            acc[m + 3] += v.w;
+                        }
+                    }
+                    // every lane has read the region before any overwrites it
+                    __syncwarp();
+                    if (j + 1 < p.splits && lane == 0)
+                        bar_arrive_cluster(peer_addr(part_free, 2u * (uint32_t)(j + 1) + r));
                 }
-                // every lane has read the region before any overwrites it
-                __syncwarp();
+                if (!got) break;
             }
             // the warp's 32 output columns (the weight rows of its accumulator
             // lanes), all mt rows: bf16 into the staging buffer, then one TMA
@@ -1017,12 +1036,13 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 bar_arrive_cluster(peer_addr(part_free, 2u + r));
             }
         }
-        // gave up with pair 1 possibly still sending this tile's partials:
-        // they land (bounded wait) before the CTA may exit
+        // gave up with the pair whose turn it is possibly still sending its
+        // partials (the others wait for a turn that does not come): they
+        // land (bounded wait) before the CTA may exit
         if (tile < p.n_tiles && p.splits > 1 && adder && warp == 4) {
             if (lane == 0 && !expected) bar_expect_tx(part_full, 512u * (uint32_t)p.mt);
             __syncwarp();
-            drain_bar(part_full, local & 1u);
+            drain_bar(part_full, pending & 1u);
         }
         // the stores have completed before the CTA exits
         if (lane == 0) bulk_wait_all();
@@ -1227,15 +1247,18 @@ int prepare_skinny(SkinnyParams* p, const uint8_t* a, const uint8_t* sfa, const 
     p->mt = mt;
     p->n_tiles = (int32_t)((N + 255) / 256);
     p->k_tiles = (int32_t)k_tiles;
-    // the K split: the fewest waves of output blocks times K steps per pair
-    // (ties to fewer pairs), every range non-empty
+    // the K split: the fewest waves of output blocks times K steps per pair,
+    // each of the splits - 1 hand-overs of partial sums counted as K steps
+    // (measured on graph replays: about 8 at mt <= 64, 16 at mt = 128), ties
+    // to fewer pairs, every range non-empty
+    const int64_t exchange = mt <= 64 ? 8 : 16;
     int best = 1;
     int64_t best_cost = -1;
     for (int splits = 1; splits <= kSkMaxSplits && splits <= k_tiles; ++splits) {
         const int resident = skinny_resident(mt, splits);
         if (resident < 1) break;
         const int64_t waves = (p->n_tiles + resident - 1) / resident;
-        const int64_t cost = waves * ((k_tiles + splits - 1) / splits);
+        const int64_t cost = waves * ((k_tiles + splits - 1) / splits + (splits - 1) * exchange);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
             best = splits;

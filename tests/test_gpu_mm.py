@@ -40,15 +40,18 @@ def _abs_bound(x, w):
                                    # 256-column tiles, K % 128 == 32, many pairs
                                    (1000, 2064, 4000), (200, 272, 1056),
                                    # M <= 128 (the swapped-operand form): MMA
-                                   # widths 32, 64 and 128, K split over two
-                                   # pairs (few output blocks) or not, partial
-                                   # last K steps, and the first M of the
-                                   # general form
+                                   # widths 32, 64 and 128, K split over two or
+                                   # three pairs (few output blocks) or not,
+                                   # partial last K steps, and the first M of
+                                   # the general form
                                    (16, 4096, 4096), (48, 2048, 14336), (64, 1040, 896),
                                    (5, 16, 32), (17, 272, 1056), (32, 14336, 640),
                                    (64, 512, 640), (65, 512, 1024), (128, 4096, 14336),
                                    (100, 2064, 4000), (96, 16, 32), (128, 14336, 640),
-                                   (127, 1040, 896), (129, 512, 1024)])
+                                   (127, 1040, 896), (129, 512, 1024),
+                                   # K split with a partial last K step, MMA
+                                   # widths 128 and 32
+                                   (100, 2064, 14016), (17, 272, 14048), (33, 512, 4000)])
 def test_mm_matches_oracle(M, N, K):
     x = W.random_fused(M, K, seed=M + K, scale=2.0).tensors[0].x
     w = W.random_weights([(N, K)], seed=N + K).tensors[0].x
@@ -158,7 +161,8 @@ def test_mm_quantized_argument_errors():
         mx.mm_mxfp8_quantized(xq, s, torch.zeros((16, 32), dtype=torch.uint8, device="cuda"), s)
 
 
-@pytest.mark.parametrize("M,N,K", [(1000, 2064, 4000), (16, 4096, 4096), (128, 4096, 4096)])
+@pytest.mark.parametrize("M,N,K", [(1000, 2064, 4000), (16, 4096, 4096), (128, 4096, 4096),
+                                   (17, 272, 14048)])
 def test_mm_is_deterministic_across_calls_and_streams(M, N, K):
     """The GEMM accumulates every output in a fixed order (K steps in turn,
     four 32-element blocks each; with M <= 128, four or two accumulators and
