@@ -67,6 +67,9 @@ def parse():
     p.add_argument("--graph", action="store_true",
                    help="capture one step in a CUDA graph and time graph replays (removes the "
                         "Python call overhead that dominates the tiny workloads)")
+    p.add_argument("--vs-cublaslt", action="store_true",
+                   help="with --mm: also time cuBLASLt's block-scaled MXFP8 GEMM "
+                        "(torch._scaled_mm) on the same quantized operands, for comparison")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     p.add_argument("--cpu-rows", type=int, default=8192,
@@ -462,6 +465,50 @@ def run_mm(args, world, rank, local, pg):
     gemm_ms = timed(gemm)
     clocks.mark("end")
     clk = clocks.stop()
+
+    def replay_us(fn, calls=20, reps=5):
+        """µs per call of fn(stream) from replays of a CUDA graph of `calls`
+        calls (back to back: operands that fit stay partly in L2)."""
+        side = torch.cuda.Stream(device)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fn(side)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(calls):
+                    fn(side)
+        stream.wait_stream(side)
+        graph.replay()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) * 1e3 / (reps * calls)
+
+    extra = {}
+    if args.graph:
+        extra["gemm_graph_replay_us"] = replay_us(
+            lambda st: mx.mm_mxfp8_quantized(xq.q_row, xq.s_row, wq.q_row, wq.s_row, out=out,
+                                             stream=st))
+    if args.vs_cublaslt:
+        e8 = torch.float8_e8m0fnu
+
+        def cub(st=None):
+            with torch.cuda.stream(st if st is not None else stream):
+                return torch._scaled_mm(xq.q_row.view(torch.float8_e4m3fn),
+                                        wq.q_row.view(torch.float8_e4m3fn).t(),
+                                        xq.s_row.view(e8), wq.s_row.view(e8),
+                                        out_dtype=torch.bfloat16)
+        for _ in range(3):
+            cub()
+        extra["cublaslt"] = {"kernel": "torch._scaled_mm (cuBLASLt block-scaled MXFP8) on the "
+                                       "same quantized operands and tiled scales",
+                             "avg_launch_us": timed(cub) * 1e3}
+        if args.graph:
+            extra["cublaslt"]["graph_replay_us"] = replay_us(cub)
     status = mx.device_status()
     if status != 0:
         raise SystemExit(f"the GEMM reported device status {status:#x}")
@@ -525,7 +572,7 @@ def run_mm(args, world, rank, local, pg):
                               if flush is not None else
                               "operands larger than L2 (%.0f MB); no flush" % (in_bytes / 1e6))},
             "roofline": roof,
-            "clocks": clk, "gpu_launches": 2 * args.steps}), flush=True)
+            "clocks": clk, "gpu_launches": 2 * args.steps, **extra}), flush=True)
     return 0
 
 
