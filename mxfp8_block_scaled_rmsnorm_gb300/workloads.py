@@ -158,6 +158,27 @@ def stress(R: int, C: int, rng=None, seed: int = 3) -> Workload:
                     [Tensor2D(bits, to_bf16_bits(g), 1e-6, 0.0)])
 
 
+def wide_range(R: int, C: int, seed: int) -> np.ndarray:
+    """bf16 bits [R, C] (C a multiple of 32, any R): N(0, 1) rows scaled by
+    2^k, k uniform in [-60, 60] per row, with 2 % of the 32-element blocks
+    zero and 2 % sub-normal (random signs and fractions)."""
+    rng = np.random.default_rng(seed)
+    x = _normal(rng, (R, C))
+    k = rng.integers(-60, 61, size=R)
+    x *= np.ldexp(np.float32(1.0), k.astype(np.int32)).astype(np.float32)[:, None]
+    bits = to_bf16_bits(x)
+    nblocks = R * C // BLOCK
+    nsel = max(1, int(0.02 * nblocks)) if nblocks >= 4 else 0
+    if nsel:
+        sel = rng.choice(nblocks, size=2 * nsel, replace=False)
+        blk = bits.reshape(nblocks, BLOCK)
+        blk[sel[:nsel]] = 0
+        sub_frac = rng.integers(1, 128, size=(nsel, BLOCK)).astype(np.uint16)
+        sub_sign = rng.integers(0, 2, size=(nsel, BLOCK)).astype(np.uint16) << 15
+        blk[sel[nsel:]] = sub_sign | sub_frac
+    return bits
+
+
 def random_fused(R: int, C: int, seed: int, scale: float = 1.0, eps: float = 1e-6,
                  offset: float = 0.0, rowwise=True, columnwise=True) -> Workload:
     rng = np.random.default_rng(seed)

@@ -122,7 +122,8 @@ def test_mm_argument_errors():
     assert e.value.code == -2
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 512, 4096), (200, 272, 1056), (33, 16, 32)])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 4096), (200, 272, 1056), (33, 16, 32),
+                                   (16, 4096, 4096), (64, 2064, 14016)])
 def test_norm_quant_feeds_gemm(M, N, K):
     """rmsnorm_quant_mxfp8 with tiled scales, then mm_mxfp8_quantized on its
     rowwise plane: the activation codes match the oracle's quantize of the
@@ -181,3 +182,26 @@ def test_mm_is_deterministic_across_calls_and_streams(M, N, K):
     assert mx.device_status() == 0
     assert torch.equal(first.view(torch.int16), again.view(torch.int16))
     assert torch.equal(first.view(torch.int16), third.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 16, 32), (5, 272, 1056), (16, 4096, 4096), (31, 512, 640),
+                                   (32, 1040, 896), (33, 2064, 4000), (48, 2048, 14336),
+                                   (63, 272, 14048), (64, 14336, 640), (64, 512, 8192)])
+def test_mm_equals_quantize_then_quantized_gemm(M, N, K):
+    """mm_mxfp8 on bf16 x gives the bytes of quant_mxfp8 (tiled scales)
+    followed by mm_mxfp8_quantized, and that quantize equals the oracle's bit
+    for bit, at decode-sized M (the swapped-operand form, with and without a
+    K split). Rows of x are scaled by 2^-60 .. 2^60, with zero and sub-normal
+    blocks, so that scale bytes across the range, the zero-scale rule and
+    saturation are all taken."""
+    x_bits = W.wide_range(M, K, seed=M * 7 + K)
+    x = to_dev(x_bits)
+    wq = mx.quantize_weight_for_mm(to_dev(W.random_weights([(N, K)], seed=N + K).tensors[0].x))
+    fused = mx.mm_mxfp8(x, wq.q_row, wq.s_row)
+    xq = mx.quant_mxfp8(x, True, False, scale_layout="mma")
+    two = mx.mm_mxfp8_quantized(xq.q_row, xq.s_row, wq.q_row, wq.s_row)
+    sync()
+    assert mx.device_status() == 0
+    qx, _, _, _ = oracle.quant_mxfp8(x_bits, True, False)
+    assert np.array_equal(xq.q_row.cpu().numpy(), qx)
+    assert torch.equal(fused.view(torch.int16), two.view(torch.int16))
