@@ -21,12 +21,13 @@ struct GemmParams {
     int32_t num_tiles;                  // m_tiles * n_tiles output tiles (one per CTA pair)
 };
 
-// The form for few activation rows (M <= kSkinnyMaxM): the operands swap
+// The form for few activation rows (M <= 64, and up to kSkinnyMaxM where it
+// is estimated faster than the general form's few 256 x 256 tiles): the operands swap
 // roles, so that the weight's rows fill the MMA's 256 rows and the activation
 // rows are its N (32, 64 or 128); the K steps of a 256-column output block are
 // split over the CTA pairs of one cluster, whose float32 partial sums meet in
 // distributed shared memory.
-constexpr int64_t kSkinnyMaxM = 128;
+constexpr int64_t kSkinnyMaxM = 2048;
 struct SkinnyParams {
     CUtensorMap tma_w;     // B codes [N, K] (the weight), boxes 128 B x 128 rows
     CUtensorMap tma_x;     // A codes [M, K] (the activation), boxes 128 B x mt/2 rows
@@ -34,10 +35,15 @@ struct SkinnyParams {
     CUtensorMap tma_sfx;   // A scales, same view
     CUtensorMap tma_out;   // bf16 output [M, N] (row-major), boxes 32 columns x mt rows
     int32_t M, N, K;
-    int32_t mt;               // activation rows per MMA (32, 64 or 128, >= M)
+    int32_t mt;               // activation rows per MMA (32, 64 or 128)
+    int32_t m_blocks;         // blocks of mt activation rows (1 unless mt = 128)
     int32_t n_tiles, k_tiles; // 256-column output blocks; 128-byte K steps
+    int32_t num_tiles;        // n_tiles * m_blocks work tiles, block n of tile t:
+                              // t / m_blocks, activation block t % m_blocks
     int32_t splits;           // CTA pairs per cluster, each taking one K range
     int32_t steps_per_split;  // K steps per range (the last range may be shorter)
+    int32_t resident;         // (planning) clusters of the chosen split held at once
+    int64_t cost;             // (planning) waves x (K steps per pair + hand-overs)
 };
 
 struct GemmPlan {

@@ -792,7 +792,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         // stream (which may have written A, B or their scales): nothing is
         // read before it has completed; the set-up above overlapped its tail
         asm volatile("griddepcontrol.wait;" ::: "memory");
-        for (int tile = cluster; ok && tile < p.n_tiles; tile += clusters) {
+        for (int tile = cluster; ok && tile < p.num_tiles; tile += clusters) {
+            const int n_blk = tile / p.m_blocks, mb = tile % p.m_blocks;
             for (int ks = k0; ks < k1; ks += kSkSub) {
                 if (!wait_bar_warp(empty(s), ph ^ 1u, abort, kSiteEmpty)) {
                     ok = false;
@@ -806,11 +807,11 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                         const int kt = ks + j;
                         const uint32_t sf = sbase + L::kOffSf + s * L::kSfStage + j * kSkSf;
                         tma_load_2d(sbase + s * L::kStageW + j * kSkTileW, &p.tma_w, kt * kBK,
-                                    tile * 256 + (int)r * 128, fb);
+                                    n_blk * 256 + (int)r * 128, fb);
                         tma_load_2d(sbase + L::kOffX + s * L::kStageX + j * L::kTileX, &p.tma_x,
-                                    kt * kBK, (int)(r * x_rows), fb);
-                        tma_load_3d(sf, &p.tma_sfw, 0, kt, 2 * tile + (int)r, fb);
-                        tma_load_3d(sf + 512, &p.tma_sfx, 0, kt, 0, fb);
+                                    kt * kBK, mb * p.mt + (int)(r * x_rows), fb);
+                        tma_load_3d(sf, &p.tma_sfw, 0, kt, 2 * n_blk + (int)r, fb);
+                        tma_load_3d(sf + 512, &p.tma_sfx, 0, kt, mb, fb);
                     }
                 }
                 __syncwarp();
@@ -851,7 +852,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         const int full_steps = p.K / kBK;  // K steps with all four 32-element blocks
         const uint64_t dsf = umma::scale_tile_desc(sbase + L::kOffSf);
         const uint32_t sf_lo0 = (uint32_t)dsf, sf_hi = (uint32_t)(dsf >> 32);
-        for (int tile = cluster; ok && tile < p.n_tiles; tile += clusters, ++local) {
+        for (int tile = cluster; ok && tile < p.num_tiles; tile += clusters, ++local) {
             if (!wait_bar_warp(tmem_empty, (local & 1u) ^ 1u, abort, kSiteTmemEmpty)) {
                 ok = false;
                 break;
@@ -939,7 +940,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         uint32_t pending = 0;   // pair 0: the receive phase waited for next
         bool expected = false;  // pair 0: that phase's bytes announced
         int tile = cluster;
-        for (; tile < p.n_tiles; tile += clusters, ++local) {
+        for (; tile < p.num_tiles; tile += clusters, ++local) {
             pending = local * sends;
             expected = false;
             const bool ok = wait_bar(tmem_full, local & 1u, abort, kSiteTmemFull);
@@ -1018,7 +1019,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             // the warp's 32 output columns (the weight rows of its accumulator
             // lanes), all mt rows: bf16 into the staging buffer, then one TMA
             // store of the box, which the tensor map clips at M and N
-            const int64_t n0 = (int64_t)tile * 256 + 128 * (int)r + 32 * q;
+            const int64_t n0 = (int64_t)(tile / p.m_blocks) * 256 + 128 * (int)r + 32 * q;
+            const int32_t m0 = (tile % p.m_blocks) * p.mt;
             if (lane == 0) bulk_wait_read<0>();  // the previous tile's store has read it
             __syncwarp();
 #pragma unroll
@@ -1027,7 +1029,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0 && n0 < p.N) {
-                tma_store_2d(&p.tma_out, stage, (int32_t)n0, 0);
+                tma_store_2d(&p.tma_out, stage, (int32_t)n0, m0);
                 bulk_commit();
             }
             if (p.splits > 1 && lane == 0) {
@@ -1039,7 +1041,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         // gave up with the pair whose turn it is possibly still sending its
         // partials (the others wait for a turn that does not come): they
         // land (bounded wait) before the CTA may exit
-        if (tile < p.n_tiles && p.splits > 1 && adder && warp == 4) {
+        if (tile < p.num_tiles && p.splits > 1 && adder && warp == 4) {
             if (lane == 0 && !expected) bar_expect_tx(part_full, 512u * (uint32_t)p.mt);
             __syncwarp();
             drain_bar(part_full, pending & 1u);
@@ -1245,8 +1247,10 @@ int prepare_skinny(SkinnyParams* p, const uint8_t* a, const uint8_t* sfa, const 
     p->N = (int32_t)N;
     p->K = (int32_t)K;
     p->mt = mt;
+    p->m_blocks = (int32_t)((M + mt - 1) / mt);
     p->n_tiles = (int32_t)((N + 255) / 256);
     p->k_tiles = (int32_t)k_tiles;
+    p->num_tiles = p->n_tiles * p->m_blocks;
     // the K split: the fewest waves of output blocks times K steps per pair,
     // each of the splits - 1 hand-overs of partial sums counted as K steps
     // (measured on graph replays: about 8 at mt <= 64, 16 at mt = 128), ties
@@ -1254,35 +1258,31 @@ int prepare_skinny(SkinnyParams* p, const uint8_t* a, const uint8_t* sfa, const 
     const int64_t exchange = mt <= 64 ? 8 : 16;
     int best = 1;
     int64_t best_cost = -1;
+    p->resident = 0;
     for (int splits = 1; splits <= kSkMaxSplits && splits <= k_tiles; ++splits) {
         const int resident = skinny_resident(mt, splits);
         if (resident < 1) break;
-        const int64_t waves = (p->n_tiles + resident - 1) / resident;
+        const int64_t waves = (p->num_tiles + resident - 1) / resident;
         const int64_t cost = waves * ((k_tiles + splits - 1) / splits + (splits - 1) * exchange);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
             best = splits;
+            p->resident = resident;
         }
     }
     const int64_t per = (k_tiles + best - 1) / best;
     p->steps_per_split = (int32_t)per;
     p->splits = (int32_t)((k_tiles + per - 1) / per);
+    p->cost = best_cost < 0 ? 0 : best_cost;
     return 0;
 }
 
-int launch_general(const GemmParams& p, void* stream) {
-    // pairs the device holds at once (the persistent grid: a pair that had to
-    // wait for another to finish would run its whole share of tiles late)
-    static int resident[kMaxDevices] = {0};
-    int dev = 0;
-    int err = (int)cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
+// Launch configuration of the general form (clusters of one CTA pair).
+cudaLaunchConfig_t general_config(cudaLaunchAttribute* attrs, void* stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attrs[2];
     attrs[0].id = cudaLaunchAttributeClusterDimension;
     attrs[0].val.clusterDim.x = 2;
     attrs[0].val.clusterDim.y = 1;
@@ -1292,22 +1292,43 @@ int launch_general(const GemmParams& p, void* stream) {
     attrs[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attrs;
     cfg.numAttrs = 2;
-    if (resident[dev] == 0) {
-        err = (int)cudaFuncSetAttribute(mxfp8_gemm_kernel,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kSmemBytes);
-        if (err != cudaSuccess) return err;
-        int sms = 0, clusters = 0;
-        err = (int)cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (err != cudaSuccess) return err;
-        cfg.gridDim = dim3((unsigned)(sms & ~1), 1, 1);
-        err = (int)cudaOccupancyMaxActiveClusters(&clusters, mxfp8_gemm_kernel, &cfg);
-        if (err != cudaSuccess) return err;
-        if (clusters < 1) return (int)cudaErrorInvalidConfiguration;
-        resident[dev] = clusters;
-    }
-    const int pairs = p.num_tiles < resident[dev] ? p.num_tiles : resident[dev];
+    return cfg;
+}
+
+// CTA pairs of the general form the current device holds at once (cached per
+// device), or a negative cudaError_t.
+int general_resident() {
+    static int resident[kMaxDevices] = {0};
+    int dev = 0;
+    int err = (int)cudaGetDevice(&dev);
+    if (err != cudaSuccess) return -err;
+    if (dev < 0 || dev >= kMaxDevices) return -(int)cudaErrorInvalidDevice;
+    if (resident[dev] > 0) return resident[dev];
+    err = (int)cudaFuncSetAttribute(mxfp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemBytes);
+    if (err != cudaSuccess) return -err;
+    int sms = 0, clusters = 0;
+    err = (int)cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return -err;
+    cudaLaunchAttribute attrs[2];
+    cudaLaunchConfig_t cfg = general_config(attrs, nullptr);
+    cfg.gridDim = dim3((unsigned)(sms & ~1), 1, 1);
+    err = (int)cudaOccupancyMaxActiveClusters(&clusters, mxfp8_gemm_kernel, &cfg);
+    if (err != cudaSuccess) return -err;
+    if (clusters < 1) return -(int)cudaErrorInvalidConfiguration;
+    resident[dev] = clusters;
+    return clusters;
+}
+
+int launch_general(const GemmParams& p, void* stream) {
+    // pairs the device holds at once (the persistent grid: a pair that had to
+    // wait for another to finish would run its whole share of tiles late)
+    const int resident = general_resident();
+    if (resident < 0) return -resident;
+    const int pairs = p.num_tiles < resident ? p.num_tiles : resident;
     if (pairs <= 0) return cudaSuccess;
+    cudaLaunchAttribute attrs[2];
+    cudaLaunchConfig_t cfg = general_config(attrs, stream);
     cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
     return (int)cudaLaunchKernelEx(&cfg, mxfp8_gemm_kernel, p);
 }
@@ -1320,7 +1341,7 @@ int launch_skinny(const SkinnyParams& p, void* stream) {
         const int err = (int)cudaGetLastError();
         return err != cudaSuccess ? err : (int)cudaErrorInvalidConfiguration;
     }
-    const int clusters = p.n_tiles < resident ? p.n_tiles : resident;
+    const int clusters = p.num_tiles < resident ? p.num_tiles : resident;
     if (clusters <= 0) return cudaSuccess;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = skinny_config<MT>(p.splits, attr, stream);
@@ -1340,9 +1361,32 @@ int launch_skinny(const SkinnyParams& p, void* stream) {
 
 int gemm_plan(GemmPlan* plan, const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
               const uint8_t* sfb, uint16_t* out, int64_t M, int64_t N, int64_t K) {
-    plan->skinny = M <= kSkinnyMaxM;
-    return plan->skinny ? prepare_skinny(&plan->thin, a, sfa, b, sfb, out, M, N, K)
-                        : prepare_general(&plan->general, a, sfa, b, sfb, out, M, N, K);
+    if (M <= 64 || M > kSkinnyMaxM) {
+        plan->skinny = M <= 64;
+        return plan->skinny ? prepare_skinny(&plan->thin, a, sfa, b, sfb, out, M, N, K)
+                            : prepare_general(&plan->general, a, sfa, b, sfb, out, M, N, K);
+    }
+    // 64 < M <= kSkinnyMaxM: the form with the smaller estimate. In cycles per
+    // wave of tiles (measured on graph replays): general, 512 per 128-byte K
+    // step and 3.3k for the tile switch; skinny at mt = 128, 330 per K step
+    // (the split's hand-overs counted as K steps) and 2k for the epilogue.
+    // Past 128 rows the skinny form is taken only when its tiles (activation
+    // row blocks x weight blocks) fit in one wave: each further wave re-reads
+    // the weight, and the estimate misses that (measured: 384 x 14336 x 4096
+    // skinny in 3 waves 27.7 us, general in 2 waves 25.4 us).
+    int err = prepare_skinny(&plan->thin, a, sfa, b, sfb, out, M, N, K);
+    if (err != 0) return err;
+    const int resident = general_resident();
+    const int64_t k_tiles = (K + kBK - 1) / kBK;
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+    const int64_t general =
+        resident > 0 ? (tiles + resident - 1) / resident * (512 * k_tiles + 3300) : -1;
+    const int64_t thin_waves = (plan->thin.num_tiles + plan->thin.resident - 1) /
+                               (plan->thin.resident > 0 ? plan->thin.resident : 1);
+    const int64_t thin = 330 * plan->thin.cost + 2000 * thin_waves;
+    plan->skinny = general < 0 || (thin < general && (M <= 128 || thin_waves == 1));
+    if (plan->skinny) return 0;
+    return prepare_general(&plan->general, a, sfa, b, sfb, out, M, N, K);
 }
 
 int gemm_launch(const GemmPlan& plan, void* stream) {

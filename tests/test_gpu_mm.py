@@ -37,7 +37,12 @@ def _abs_bound(x, w):
 @pytest.mark.parametrize("M,N,K", [(256, 384, 1024), (200, 128, 512), (1, 16, 32),
                                    (33, 256, 7168), (1024, 4096, 4096),
                                    # ragged in all three: partial 256-row and
-                                   # 256-column tiles, K % 128 == 32, many pairs
+                                   # 256-column tiles, K % 128 == 32; the
+                                   # general form (M past the swapped form's
+                                   # limit, or its row blocks over more than
+                                   # one wave) and the swapped form with
+                                   # several 128-row activation blocks
+                                   (2100, 272, 1056), (2000, 2064, 4000),
                                    (1000, 2064, 4000), (200, 272, 1056),
                                    # M <= 128 (the swapped-operand form): MMA
                                    # widths 32, 64 and 128, K split over two or
@@ -51,7 +56,9 @@ def _abs_bound(x, w):
                                    (127, 1040, 896), (129, 512, 1024),
                                    # K split with a partial last K step, MMA
                                    # widths 128 and 32
-                                   (100, 2064, 14016), (17, 272, 14048), (33, 512, 4000)])
+                                   (100, 2064, 14016), (17, 272, 14048), (33, 512, 4000),
+                                   # two 128-row activation blocks and a K split
+                                   (256, 1040, 14016)])
 def test_mm_matches_oracle(M, N, K):
     x = W.random_fused(M, K, seed=M + K, scale=2.0).tensors[0].x
     w = W.random_weights([(N, K)], seed=N + K).tensors[0].x
@@ -162,8 +169,8 @@ def test_mm_quantized_argument_errors():
         mx.mm_mxfp8_quantized(xq, s, torch.zeros((16, 32), dtype=torch.uint8, device="cuda"), s)
 
 
-@pytest.mark.parametrize("M,N,K", [(1000, 2064, 4000), (16, 4096, 4096), (128, 4096, 4096),
-                                   (17, 272, 14048)])
+@pytest.mark.parametrize("M,N,K", [(2100, 272, 1056), (1000, 2064, 4000), (16, 4096, 4096),
+                                   (128, 4096, 4096), (17, 272, 14048)])
 def test_mm_is_deterministic_across_calls_and_streams(M, N, K):
     """The GEMM accumulates every output in a fixed order (K steps in turn,
     four 32-element blocks each; with M <= 128, four or two accumulators and
