@@ -57,12 +57,14 @@
 //    pair's copies and MMAs in flight, and both CTAs meet at a cluster barrier,
 //    free their tensor memory and exit.
 //
-// Skinny form (M <= 128 activation rows, e.g. decoding steps): a 256-row
-// output tile would be mostly empty, and few tiles would leave most SMs idle,
-// so the operands swap roles. The weight's 256-row block fills the MMA's M
-// (128 rows per CTA of the pair) and the activation rows are its N (32, 64
-// or 128, zero rows past M), so out^T is accumulated: weight row n in
-// tensor-memory lane n, activation row m in column m. The tensor cores have
+// Skinny form (decoding steps, M <= 64, and mid-size M where the planner
+// estimates it faster): a 256-row output tile would be mostly empty, and few
+// tiles would leave most SMs idle, so the operands swap roles. The weight's
+// 256-row block fills the MMA's M (128 rows per CTA of the pair) and the
+// activation rows are its N (32, 64 or 128, zero rows past M; more rows run
+// as several 128-row activation blocks, each a work tile), so out^T is
+// accumulated: weight row n in tensor-memory lane n, activation row m in
+// column m. The tensor cores have
 // little to do and the kernel streams the weight; what bounds it is the MMA
 // warp's issue rate, so a stage holds two K steps (one wait and one commit
 // per eight MMAs) and the four 32-element blocks of a K step add into four
@@ -707,9 +709,10 @@ __device__ __forceinline__ uint16_t bf16_rn(float v) {
     return r;
 }
 
-// out[M, N] for M <= kSkinnyMaxM. Cluster c takes the 256-column output
-// blocks c, c + clusters, ...; pair j of the cluster (CTA ranks 2j, 2j + 1)
-// accumulates the K steps [j * steps_per_split, ...) of the block: weight
+// out[M, N] for M <= kSkinnyMaxM. Cluster c takes the work tiles c,
+// c + clusters, ... (tile t: 256-column output block t / m_blocks, activation
+// rows mt (t % m_blocks) ..); pair j of the cluster (CTA ranks 2j, 2j + 1)
+// accumulates the K steps [j * steps_per_split, ...) of the tile: weight
 // rows 128 r .. of the block in CTA r's tensor-memory lanes, activation row m
 // in column m of each accumulator (the 32-element blocks of a K step spread
 // over kChains of them). With one pair the epilogue adds the accumulators and
