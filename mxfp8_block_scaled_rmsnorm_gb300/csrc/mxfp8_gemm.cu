@@ -1235,17 +1235,14 @@ int skinny_resident(int mt, int splits) {
     return mt <= 64 ? skinny_resident<64>(splits) : skinny_resident<128>(splits);
 }
 
-int prepare_skinny(SkinnyParams* p, const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
-                   const uint8_t* sfb, uint16_t* out, int64_t M, int64_t N, int64_t K) {
+// The skinny form's shape, K split and cost estimate for M x N x K (no
+// tensor maps): the split is the one with the fewest waves of work tiles
+// times K steps per pair, each of the splits - 1 hand-overs of partial sums
+// counted as K steps (measured on graph replays: about 8 at mt <= 64, 16 at
+// mt = 128), ties to fewer pairs, every range non-empty.
+void plan_skinny(SkinnyParams* p, int64_t M, int64_t N, int64_t K) {
     const int64_t k_tiles = (K + kBK - 1) / kBK;
     const int mt = M <= 32 ? 32 : M <= 64 ? 64 : 128;
-    if (encode_operand(&p->tma_x, a, M, K, (uint32_t)mt / 2) != 0 ||
-        encode_scales(&p->tma_sfx, sfa, M, k_tiles, 1))
-        return -1;
-    if (encode_operand(&p->tma_w, b, N, K) != 0 || encode_scales(&p->tma_sfw, sfb, N, k_tiles, 1))
-        return -2;
-    if (encode_output(&p->tma_out, out, M, N, (uint32_t)mt, CU_TENSOR_MAP_SWIZZLE_NONE) != 0)
-        return -3;
     p->M = (int32_t)M;
     p->N = (int32_t)N;
     p->K = (int32_t)K;
@@ -1254,10 +1251,6 @@ int prepare_skinny(SkinnyParams* p, const uint8_t* a, const uint8_t* sfa, const 
     p->n_tiles = (int32_t)((N + 255) / 256);
     p->k_tiles = (int32_t)k_tiles;
     p->num_tiles = p->n_tiles * p->m_blocks;
-    // the K split: the fewest waves of output blocks times K steps per pair,
-    // each of the splits - 1 hand-overs of partial sums counted as K steps
-    // (measured on graph replays: about 8 at mt <= 64, 16 at mt = 128), ties
-    // to fewer pairs, every range non-empty
     const int64_t exchange = mt <= 64 ? 8 : 16;
     int best = 1;
     int64_t best_cost = -1;
@@ -1277,6 +1270,19 @@ int prepare_skinny(SkinnyParams* p, const uint8_t* a, const uint8_t* sfa, const 
     p->steps_per_split = (int32_t)per;
     p->splits = (int32_t)((k_tiles + per - 1) / per);
     p->cost = best_cost < 0 ? 0 : best_cost;
+}
+
+// The tensor maps of a planned skinny form.
+int encode_skinny(SkinnyParams* p, const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
+                  const uint8_t* sfb, uint16_t* out) {
+    const int64_t M = p->M, N = p->N, K = p->K, k_tiles = p->k_tiles;
+    if (encode_operand(&p->tma_x, a, M, K, (uint32_t)p->mt / 2) != 0 ||
+        encode_scales(&p->tma_sfx, sfa, M, k_tiles, 1))
+        return -1;
+    if (encode_operand(&p->tma_w, b, N, K) != 0 || encode_scales(&p->tma_sfw, sfb, N, k_tiles, 1))
+        return -2;
+    if (encode_output(&p->tma_out, out, M, N, (uint32_t)p->mt, CU_TENSOR_MAP_SWIZZLE_NONE) != 0)
+        return -3;
     return 0;
 }
 
@@ -1364,10 +1370,14 @@ int launch_skinny(const SkinnyParams& p, void* stream) {
 
 int gemm_plan(GemmPlan* plan, const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
               const uint8_t* sfb, uint16_t* out, int64_t M, int64_t N, int64_t K) {
-    if (M <= 64 || M > kSkinnyMaxM) {
-        plan->skinny = M <= 64;
-        return plan->skinny ? prepare_skinny(&plan->thin, a, sfa, b, sfb, out, M, N, K)
-                            : prepare_general(&plan->general, a, sfa, b, sfb, out, M, N, K);
+    if (M > kSkinnyMaxM) {
+        plan->skinny = false;
+        return prepare_general(&plan->general, a, sfa, b, sfb, out, M, N, K);
+    }
+    plan_skinny(&plan->thin, M, N, K);
+    if (M <= 64) {
+        plan->skinny = true;
+        return encode_skinny(&plan->thin, a, sfa, b, sfb, out);
     }
     // 64 < M <= kSkinnyMaxM: the form with the smaller estimate. In cycles per
     // wave of tiles (measured on graph replays): general, 512 per 128-byte K
@@ -1377,8 +1387,6 @@ int gemm_plan(GemmPlan* plan, const uint8_t* a, const uint8_t* sfa, const uint8_
     // row blocks x weight blocks) fit in one wave: each further wave re-reads
     // the weight, and the estimate misses that (measured: 384 x 14336 x 4096
     // skinny in 3 waves 27.7 us, general in 2 waves 25.4 us).
-    int err = prepare_skinny(&plan->thin, a, sfa, b, sfb, out, M, N, K);
-    if (err != 0) return err;
     const int resident = general_resident();
     const int64_t k_tiles = (K + kBK - 1) / kBK;
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
@@ -1388,8 +1396,8 @@ int gemm_plan(GemmPlan* plan, const uint8_t* a, const uint8_t* sfa, const uint8_
                                (plan->thin.resident > 0 ? plan->thin.resident : 1);
     const int64_t thin = 330 * plan->thin.cost + 2000 * thin_waves;
     plan->skinny = general < 0 || (thin < general && (M <= 128 || thin_waves == 1));
-    if (plan->skinny) return 0;
-    return prepare_general(&plan->general, a, sfa, b, sfb, out, M, N, K);
+    return plan->skinny ? encode_skinny(&plan->thin, a, sfa, b, sfb, out)
+                        : prepare_general(&plan->general, a, sfa, b, sfb, out, M, N, K);
 }
 
 int gemm_launch(const GemmPlan& plan, void* stream) {
