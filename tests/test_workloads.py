@@ -52,3 +52,23 @@ def test_random_bits_recipe():
     sign = a.x >> 15
     assert 0.4 < sign.mean() < 0.6
     assert len(np.unique(a.x & 0x7F)) == 128
+
+
+def test_wide_range_recipe():
+    """Any row count; 2 % zero and 2 % sub-normal 32-element blocks, disjoint;
+    rows 2^k-scaled with k in [-60, 60], so block exponents span far more than
+    E4M3's range; the same seed gives the same bytes."""
+    R, C = 37, 4096
+    a = W.wide_range(R, C, seed=5)
+    assert a.shape == (R, C) and a.dtype == np.uint16
+    assert np.array_equal(a, W.wide_range(R, C, seed=5))
+    assert not np.array_equal(a, W.wide_range(R, C, seed=6))
+    blk = a.reshape(-1, 32)
+    nsel = max(1, int(0.02 * blk.shape[0]))
+    zero = np.all(blk == 0, axis=1)
+    expo = (blk >> 7) & 0xFF
+    sub = np.all((expo == 0) & ((blk & 0x7F) != 0), axis=1)
+    assert zero.sum() == nsel and sub.sum() == nsel and not np.any(zero & sub)
+    row_max = expo.reshape(R, -1).max(axis=1)
+    assert row_max.max() - row_max.min() > 60
+    assert W.wide_range(1, 32, seed=1).shape == (1, 32)
