@@ -42,7 +42,7 @@ def _abs_bound(x, w):
                                    # limit, or its row blocks over more than
                                    # one wave) and the swapped form with
                                    # several 128-row activation blocks
-                                   (2100, 272, 1056), (2000, 2064, 4000),
+                                   (2100, 272, 1056), (2000, 2064, 4000), (2100, 16, 32),
                                    (1000, 2064, 4000), (200, 272, 1056),
                                    # M <= 128 (the swapped-operand form): MMA
                                    # widths 32, 64 and 128, K split over two or
