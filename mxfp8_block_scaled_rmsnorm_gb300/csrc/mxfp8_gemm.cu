@@ -68,7 +68,7 @@
 // little to do and the kernel streams the weight; what bounds it is the MMA
 // warp's issue rate, so a stage holds two K steps (one wait and one commit
 // per eight MMAs) and the four 32-element blocks of a K step add into four
-// separate accumulators (two for N = 128; summed by the epilogue; MMAs into
+// separate accumulators (one for N = 128; summed by the epilogue; MMAs into
 // one accumulator wait for each other). With few output blocks the K range is
 // split over two or three pairs of a cluster; in turn, each CTA of a later
 // pair writes its float32 partial straight into the shared memory of the
@@ -154,8 +154,9 @@ struct SkLayout {
     // accumulator k % kChains, at columns MT * (k % kChains) ..): MMAs into one
     // accumulator wait for each other, and with mt <= 64 columns each is too
     // short to hide that (a K step took as long as a 256-column one); the
-    // epilogue adds the accumulators. Four of 64 columns, or two of 128.
-    static constexpr int kChains = 256 / MT;
+    // epilogue adds the accumulators. Four of 64 columns; at 128 columns one
+    // (measured 1-2 % faster than two, which had been faster than three).
+    static constexpr int kChains = MT <= 64 ? 4 : 1;
     static constexpr uint32_t kColSfw = kChains * MT;                  // 4 columns per K step
     static constexpr uint32_t kColSfx = kColSfw + 4 * kSkSub * kStages;  // 4 columns per K step
     static_assert(8 * kNumBars + 8 <= kBarBytes, "barriers, tensor-memory slot, abort flag");

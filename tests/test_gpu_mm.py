@@ -173,7 +173,7 @@ def test_mm_quantized_argument_errors():
                                    (128, 4096, 4096), (17, 272, 14048)])
 def test_mm_is_deterministic_across_calls_and_streams(M, N, K):
     """The GEMM accumulates every output in a fixed order (K steps in turn,
-    four 32-element blocks each; with M <= 128, four or two accumulators and
+    four 32-element blocks each; in the swapped-operand form, four accumulators or one and
     the K split's partial sums added in pair order), so repeated calls give the same
     bytes, on the default stream and on a side stream alike."""
     x = to_dev(W.random_fused(M, K, seed=11, scale=2.0).tensors[0].x)
