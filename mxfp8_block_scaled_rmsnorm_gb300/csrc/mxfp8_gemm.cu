@@ -622,6 +622,11 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
             // tensor-memory loads need) only if all lanes saw the phase complete
             const bool ok = wait_bar(tmem_full, local & 1u, abort, kSiteTmemFull);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            // the CTA's last accumulator is complete: a GEMM launched after
+            // this one as a programmatic dependent may start its set-up (it
+            // reads and writes nothing before this grid has completed)
+            if (tile + pairs >= p.num_tiles)
+                asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             tc_fence_after();
             uint32_t packed[64];
 #pragma unroll
@@ -949,6 +954,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             expected = false;
             const bool ok = wait_bar(tmem_full, local & 1u, abort, kSiteTmemFull);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            // the CTA's last accumulator is complete: a dependent GEMM may
+            // start its set-up (as in the general form)
+            if (tile + clusters >= p.num_tiles)
+                asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             tc_fence_after();
             // accumulator 0 straight into acc (all its loads in flight), the
             // others added 32 columns at a time (columns past mt are not read)
