@@ -283,10 +283,18 @@ int64_t mxfp8_device_status(int clear);
  *   MXFP8_HOOK_MAX_CLUSTER  value > 0: the fused calls use thread-block
  *       clusters of at most `value` CTAs (1: one CTA per 32-row stripe, the
  *       path taken where the device co-schedules no cluster); 0 lifts the cap.
+ *   MXFP8_HOOK_GEMM_FORM  the form of the matrix multiplies: 1 the 256 x 256
+ *       output-tile form, 2 the swapped-operand form (where M <= 2048; the
+ *       tile form above), 0 the planner's choice.
+ *   MXFP8_HOOK_GEMM_SPLITS  value 1-3: the swapped-operand form splits K over
+ *       that many CTA pairs (fewer where K has fewer 128-element steps);
+ *       0 the planner's choice. Larger values are rejected.
  * Returns the hook's previous value, or MXFP8_ERR_FLAGS for an unknown hook
- * or a negative value. Not meant to be set while other threads call. */
+ * or a value out of range. Not meant to be set while other threads call. */
 #define MXFP8_HOOK_FAIL_LAUNCH 1
 #define MXFP8_HOOK_MAX_CLUSTER 2
+#define MXFP8_HOOK_GEMM_FORM 3
+#define MXFP8_HOOK_GEMM_SPLITS 4
 int mxfp8_set_test_hook(int hook, int value);
 
 /* Text of the last error raised by a call on this host thread ("" if none).

@@ -69,4 +69,11 @@ int gemm_launch(const GemmPlan& plan, void* stream);
 // cleared), read with a synchronizing copy; cleared when asked.
 int gemm_status(bool clear, unsigned long long* out);
 
+// Test hooks (mxfp8_set_test_hook, mxfp8_api.cu): the form the planner is
+// held to (0 its own choice, 1 the 256 x 256-tile form, 2 the swapped form
+// where M <= kSkinnyMaxM) and the K split of the swapped form (0 its own
+// choice, else that many pairs, at most the K steps).
+int hook_gemm_form();
+int hook_gemm_splits();
+
 }  // namespace mx

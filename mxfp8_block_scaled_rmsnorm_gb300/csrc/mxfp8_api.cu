@@ -192,6 +192,8 @@ namespace mx {
 namespace {
 std::atomic<int> g_hook_fail_launch{0};
 std::atomic<int> g_hook_max_cluster{0};
+std::atomic<int> g_hook_gemm_form{0};
+std::atomic<int> g_hook_gemm_splits{0};
 }  // namespace
 
 int hook_launch_error() {
@@ -199,6 +201,8 @@ int hook_launch_error() {
                                                               : (int)cudaSuccess;
 }
 int hook_max_cluster() { return g_hook_max_cluster.load(std::memory_order_relaxed); }
+int hook_gemm_form() { return g_hook_gemm_form.load(std::memory_order_relaxed); }
+int hook_gemm_splits() { return g_hook_gemm_splits.load(std::memory_order_relaxed); }
 
 TraceRange::TraceRange(const char* name) { nvtxRangePushA(name); }
 TraceRange::~TraceRange() { nvtxRangePop(); }
@@ -350,6 +354,12 @@ int mxfp8_set_test_hook(int hook, int value) {
             return mx::g_hook_fail_launch.exchange(value != 0 ? 1 : 0);
         case MXFP8_HOOK_MAX_CLUSTER:
             return mx::g_hook_max_cluster.exchange(value);
+        case MXFP8_HOOK_GEMM_FORM:
+            if (value > 2) return fail(MXFP8_ERR_FLAGS, "GEMM form hook: %d is not 0, 1 or 2", value);
+            return mx::g_hook_gemm_form.exchange(value);
+        case MXFP8_HOOK_GEMM_SPLITS:
+            if (value > 3) return fail(MXFP8_ERR_FLAGS, "GEMM split hook: %d is past 3", value);
+            return mx::g_hook_gemm_splits.exchange(value);
         default:
             return fail(MXFP8_ERR_FLAGS, "unknown test hook %d", hook);
     }

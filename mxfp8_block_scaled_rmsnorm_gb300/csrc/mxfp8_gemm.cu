@@ -1276,6 +1276,15 @@ void plan_skinny(SkinnyParams* p, int64_t M, int64_t N, int64_t K) {
             p->resident = resident;
         }
     }
+    const int forced = hook_gemm_splits();
+    if (forced > 0 && forced <= kSkMaxSplits) {
+        const int f = forced < k_tiles ? forced : (int)k_tiles;
+        const int resident = skinny_resident(mt, f);
+        if (resident > 0) {
+            best = f;
+            p->resident = resident;
+        }
+    }
     const int64_t per = (k_tiles + best - 1) / best;
     p->steps_per_split = (int32_t)per;
     p->splits = (int32_t)((k_tiles + per - 1) / per);
@@ -1380,12 +1389,13 @@ int launch_skinny(const SkinnyParams& p, void* stream) {
 
 int gemm_plan(GemmPlan* plan, const uint8_t* a, const uint8_t* sfa, const uint8_t* b,
               const uint8_t* sfb, uint16_t* out, int64_t M, int64_t N, int64_t K) {
-    if (M > kSkinnyMaxM) {
+    const int form = hook_gemm_form();
+    if (form == 1 || M > kSkinnyMaxM) {
         plan->skinny = false;
         return prepare_general(&plan->general, a, sfa, b, sfb, out, M, N, K);
     }
     plan_skinny(&plan->thin, M, N, K);
-    if (M <= 64) {
+    if (M <= 64 || form == 2) {
         plan->skinny = true;
         return encode_skinny(&plan->thin, a, sfa, b, sfb, out);
     }

@@ -169,6 +169,14 @@ def test_test_hook_arguments(mx):
     assert L.mxfp8_set_test_hook(HOOK_MAX_CLUSTER, -1) == -3
     assert L.mxfp8_set_test_hook(HOOK_MAX_CLUSTER, 4) == 0
     assert L.mxfp8_set_test_hook(HOOK_MAX_CLUSTER, 0) == 4
+    # the GEMM hooks: form 0-2, split 0-3; out-of-range values change nothing
+    HOOK_GEMM_FORM, HOOK_GEMM_SPLITS = 3, 4
+    assert L.mxfp8_set_test_hook(HOOK_GEMM_FORM, 3) == -3
+    assert L.mxfp8_set_test_hook(HOOK_GEMM_FORM, 2) == 0
+    assert L.mxfp8_set_test_hook(HOOK_GEMM_FORM, 0) == 2
+    assert L.mxfp8_set_test_hook(HOOK_GEMM_SPLITS, 4) == -3
+    assert L.mxfp8_set_test_hook(HOOK_GEMM_SPLITS, 3) == 0
+    assert L.mxfp8_set_test_hook(HOOK_GEMM_SPLITS, 0) == 3
 
 
 @pytest.mark.parametrize("fn", ["rmsnorm_quant_mxfp8", "quant_mxfp8", "mxfp8_rmsnorm_quant",

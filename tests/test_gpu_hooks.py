@@ -10,6 +10,11 @@ not produce, forced through the testing hooks of include/mxfp8norm.h.
 - A launch that the CUDA runtime rejects: every call reports MXFP8_ERR_CUDA
   with the runtime's text, and once the injection stops the same buffers work
   (the rejection is not sticky).
+- The matrix multiply in a form or K split the planner would not choose for
+  the shape: the 256 x 256-tile form for decode-sized M, the swapped-operand
+  form over several waves of tiles, and K splits whose clusters each walk
+  several output blocks (the hand-over of partial sums across tiles). Each
+  must meet the GEMM's bound against the oracle.
 """
 import ctypes
 
@@ -25,7 +30,7 @@ from parity import assert_quant_exact, check_fused, sync
 
 pytestmark = pytest.mark.gpu
 
-HOOK_FAIL_LAUNCH, HOOK_MAX_CLUSTER = 1, 2
+HOOK_FAIL_LAUNCH, HOOK_MAX_CLUSTER, HOOK_GEMM_FORM, HOOK_GEMM_SPLITS = 1, 2, 3, 4
 
 
 @pytest.fixture(scope="module")
@@ -92,3 +97,32 @@ def test_rejected_launch_reports_err_cuda_and_is_not_sticky(lib):
     sync()
     want = oracle.quant_mxfp8(bf16_bits(out.normed))
     assert_quant_exact(tuple(u8(v) for v in out[1:]), want, "after the rejected launches")
+
+
+@pytest.mark.parametrize("M,N,K,form,splits", [
+    (16, 2064, 4000, 1, 0),    # decode-sized M in the 256 x 256-tile form
+    (300, 20480, 1056, 2, 0),  # swapped form, 3 activation blocks x 80 weight blocks: 4 waves
+    (16, 28672, 1056, 0, 3),   # three pairs per K range, 112 blocks: several per cluster
+    (200, 20480, 1056, 2, 2),  # two pairs, 2 activation blocks x 80 weight blocks
+    (64, 272, 96, 0, 3),       # one K step: the split falls back to one pair
+])
+def test_gemm_forced_form_and_split(lib, M, N, K, form, splits):
+    x = W.random_fused(M, K, seed=M + N, scale=2.0).tensors[0].x
+    w = W.random_weights([(N, K)], seed=N + K).tensors[0].x
+    wq = mx.quantize_weight_for_mm(to_dev(w))
+    prev_form = lib.mxfp8_set_test_hook(HOOK_GEMM_FORM, form)
+    prev_splits = lib.mxfp8_set_test_hook(HOOK_GEMM_SPLITS, splits)
+    try:
+        out = mx.mm_mxfp8(to_dev(x), wq.q_row, wq.s_row)
+        sync()
+    finally:
+        lib.mxfp8_set_test_hook(HOOK_GEMM_FORM, prev_form)
+        lib.mxfp8_set_test_hook(HOOK_GEMM_SPLITS, prev_splits)
+    assert mx.device_status() == 0
+    qx, sx, _, _ = oracle.quant_mxfp8(x, True, False)
+    qw, sw, _, _ = oracle.quant_mxfp8(w, True, False)
+    A, B = oracle.dequantize_rowwise(qx, sx), oracle.dequantize_rowwise(qw, sw)
+    ref = A @ B.T
+    got = out.double().cpu().numpy()
+    bound = 2.0**-8 * np.abs(ref) + 2.0**-16 * (np.abs(A) @ np.abs(B).T) + 1e-30
+    assert np.all(np.abs(got - ref) <= bound), float(np.max(np.abs(got - ref) / bound))
