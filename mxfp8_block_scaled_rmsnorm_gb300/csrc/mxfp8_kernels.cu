@@ -710,8 +710,15 @@ fused_rmsnorm_quant_kernel(const __grid_constant__ Table<MAXN> T) {
         cluster_arrive_release();
         cluster_wait_acquire();
         if (tid < kBlock) {
+            // every peer's partial in flight at once, then added in rank order
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (j < K) v[j] = ld_cluster_f32(&part[tid], (uint32_t)j);
             float s = 0.f;
-            for (int j = 0; j < K; ++j) s += ld_cluster_f32(&part[tid], (uint32_t)j);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (j < K) s += v[j];
             inv_rms[tid] = 1.0f / sqrtf(s / (float)C + D.eps);
         }
         // done reading the peers' shared memory (the loads have completed:
