@@ -347,7 +347,9 @@ def base_record(args, wl, R, C, world):
             "launch": "cuda-graph replay" if getattr(args, "graph", False) else "eager",
             "scale_layout": getattr(args, "scale_layout", "compact"),
             "residual": bool(getattr(args, "residual", False)),
-            "op": "update_planes" if getattr(args, "update", False) else "quantize",
+            "op": ("update_planes" if getattr(args, "update", False)
+                   else "add_rmsnorm_quant_mxfp8" if getattr(args, "residual", False)
+                   else "rmsnorm_quant_mxfp8" if wl.fused else "quant_mxfp8"),
         },
     }
 
