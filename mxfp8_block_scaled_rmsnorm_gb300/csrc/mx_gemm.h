@@ -43,8 +43,21 @@ struct SkinnyParams {
     int32_t splits;           // CTA pairs per cluster, each taking one K range
     int32_t steps_per_split;  // K steps per range (the last range may be shorter)
     int32_t resident;         // (planning) clusters of the chosen split held at once
+    int32_t weight_early;     // the weight and its scales may be read before the
+                              // dependency wait (see below)
     int64_t cost;             // (planning) waves x (K steps per pair + hand-overs)
 };
+
+// weight_early (0 unless the caller sets it after gemm_plan): the GEMMs are
+// launched as programmatic dependents of the kernel before them on the stream
+// and read nothing before that kernel has completed. When that kernel is
+// known to leave the weight and its scales alone, and itself started only
+// after everything before it had completed, the weight is already final when
+// the GEMM starts, so the swapped form's first ring stages of weight copies go
+// out before the wait and overlap the previous kernel. mm_mxfp8 sets it: its
+// GEMM follows its own activation quantize, an ordinary launch that writes
+// only the activation's scratch. (The 256 x 256-tile form measured no gain
+// from the same and does not take it.)
 
 struct GemmPlan {
     bool skinny;

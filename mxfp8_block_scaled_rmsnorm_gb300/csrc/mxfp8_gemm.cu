@@ -797,9 +797,34 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         uint32_t ph = 0;
         uint32_t used = 0, last_par = 0;  // per stage: filled at all; parity of its last fill
         bool ok = true;
+        // the first tile's first stages of the weight when it may be read
+        // before the wait (weight_early): the ring is empty, so these stages
+        // need no wait, and their stage byte counts are announced here
+        int early = 0;
+        if (p.weight_early && cluster < p.num_tiles) {
+            const int n_blk = cluster / p.m_blocks;
+            const int stages = (k1 - k0 + kSkSub - 1) / kSkSub;
+            early = stages < kStages ? stages : kStages;
+            for (int i = 0; i < early; ++i) {
+                const uint32_t fb = lead_full0 + 8u * (uint32_t)i;
+                if (elect_one()) {
+                    if (leader) bar_expect_tx(full(i), 2 * stage_tx);
+#pragma unroll
+                    for (int j = 0; j < kSkSub; ++j) {
+                        const int kt = k0 + i * kSkSub + j;
+                        tma_load_2d(sbase + i * L::kStageW + j * kSkTileW, &p.tma_w, kt * kBK,
+                                    n_blk * 256 + (int)r * 128, fb);
+                        tma_load_3d(sbase + L::kOffSf + i * L::kSfStage + j * kSkSf, &p.tma_sfw,
+                                    0, kt, 2 * n_blk + (int)r, fb);
+                    }
+                }
+                __syncwarp();
+                used |= 1u << i;  // first fill: parity 0
+            }
+        }
         // launched as a programmatic dependent of the previous kernel on the
-        // stream (which may have written A, B or their scales): nothing is
-        // read before it has completed; the set-up above overlapped its tail
+        // stream (which may have written A, B or their scales): nothing else
+        // is read before it has completed; the set-up above overlapped its tail
         asm volatile("griddepcontrol.wait;" ::: "memory");
         for (int tile = cluster; ok && tile < p.num_tiles; tile += clusters) {
             const int n_blk = tile / p.m_blocks, mb = tile % p.m_blocks;
@@ -809,17 +834,21 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     break;
                 }
                 const uint32_t fb = lead_full0 + 8u * (uint32_t)s;
+                // the first tile's first `early` stages already hold their weight
+                const bool w_done = tile == cluster && (ks - k0) / kSkSub < early;
                 if (elect_one()) {
-                    if (leader) bar_expect_tx(full(s), 2 * stage_tx);
+                    if (leader && !w_done) bar_expect_tx(full(s), 2 * stage_tx);
 #pragma unroll
                     for (int j = 0; j < kSkSub; ++j) {
                         const int kt = ks + j;
                         const uint32_t sf = sbase + L::kOffSf + s * L::kSfStage + j * kSkSf;
-                        tma_load_2d(sbase + s * L::kStageW + j * kSkTileW, &p.tma_w, kt * kBK,
-                                    n_blk * 256 + (int)r * 128, fb);
+                        if (!w_done) {
+                            tma_load_2d(sbase + s * L::kStageW + j * kSkTileW, &p.tma_w,
+                                        kt * kBK, n_blk * 256 + (int)r * 128, fb);
+                            tma_load_3d(sf, &p.tma_sfw, 0, kt, 2 * n_blk + (int)r, fb);
+                        }
                         tma_load_2d(sbase + L::kOffX + s * L::kStageX + j * L::kTileX, &p.tma_x,
                                     kt * kBK, mb * p.mt + (int)(r * x_rows), fb);
-                        tma_load_3d(sf, &p.tma_sfw, 0, kt, 2 * n_blk + (int)r, fb);
                         tma_load_3d(sf + 512, &p.tma_sfx, 0, kt, mb, fb);
                     }
                 }

@@ -845,6 +845,10 @@ quant_kernel(const __grid_constant__ Table<MAXN> T) {
     }
 }
 
+// An ordinary launch (no programmatic dependency on the kernel before it):
+// the kernel starts after all earlier work on the stream has completed.
+// mm_mxfp8 relies on this for its activation quantize: the GEMM after it
+// fetches the weight before its own dependency wait.
 template <typename Kern, int MAXN>
 int launch(Kern kern, const Table<MAXN>& t, int64_t grid, int threads, int cluster,
            void* stream, int smem = 0) {

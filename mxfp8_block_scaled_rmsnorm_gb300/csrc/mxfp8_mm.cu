@@ -57,6 +57,10 @@ int mm_run(const void* x, int64_t M, int64_t K, const void* w_q, const void* w_s
     if (mr != 0)
         return mx::set_error(MXFP8_ERR_CUDA, "cannot make the TMA tensor map of %s",
                              mr == -1 ? "x" : mr == -2 ? "w_q" : "out");
+    // the quantize below writes only the scratch and is an ordinary launch
+    // (it starts after all earlier work): the GEMM after it may fetch the
+    // weight before its dependency wait
+    plan.thin.weight_early = 1;
     mx::Table<mx::kSmallTable> t;
     std::memset(&t, 0, sizeof t);
     t.n = 1;

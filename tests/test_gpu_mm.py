@@ -212,3 +212,34 @@ def test_mm_equals_quantize_then_quantized_gemm(M, N, K):
     qx, _, _, _ = oracle.quant_mxfp8(x_bits, True, False)
     assert np.array_equal(xq.q_row.cpu().numpy(), qx)
     assert torch.equal(fused.view(torch.int16), two.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 14336, 4096), (1, 4096, 14336), (64, 2048, 4096),
+                                   (128, 4096, 4096)])
+def test_mm_reads_the_weight_written_just_before(M, N, K):
+    """mm_mxfp8's GEMM fetches the first ring stages of the weight before its
+    dependency wait (the activation quantize before it writes only the
+    scratch, and started after all earlier work). So a weight quantized into
+    the same buffers by the launch right before each call, with no
+    synchronization in between, must give the product of that new weight:
+    each call equals the same call repeated after everything has finished."""
+    x = to_dev(W.random_fused(M, K, seed=21, scale=1.0).tensors[0].x)
+    ws = [to_dev(W.random_weights([(N, K)], seed=30 + i).tensors[0].x) for i in range(4)]
+    wq = mx.quantize_weight_for_mm(ws[0])
+    outs = []
+    for i in range(8):
+        mx.quant_mxfp8(ws[i % 4], True, False, out=wq, scale_layout="mma")
+        outs.append(mx.mm_mxfp8(x, wq.q_row, wq.s_row))
+    sync()
+    assert mx.device_status() == 0
+    for i in range(4):
+        fresh = mx.quantize_weight_for_mm(ws[i])
+        want = mx.mm_mxfp8_quantized(*_act(x), fresh.q_row, fresh.s_row)
+        sync()
+        for j in (i, i + 4):
+            assert torch.equal(outs[j].view(torch.int16), want.view(torch.int16)), (i, j)
+
+
+def _act(x):
+    q = mx.quant_mxfp8(x, True, False, scale_layout="mma")
+    return q.q_row, q.s_row
