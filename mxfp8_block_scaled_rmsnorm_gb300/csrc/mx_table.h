@@ -103,6 +103,11 @@ int fused_chunk_cols();
 // for the fused kernel; queried once per device.
 int fused_max_cluster();
 
+// CTAs of the fused kernel the current device holds at once (SMs x CTAs per
+// SM, from the occupancy calculator); queried once per device, 0 if the query
+// fails.
+int fused_resident_ctas();
+
 // Status word of the bounds-checking build (always 0 in the normal build),
 // read with a synchronizing copy; cleared when asked.
 int bounds_status(bool clear, unsigned long long* out);

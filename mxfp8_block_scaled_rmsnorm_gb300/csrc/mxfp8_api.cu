@@ -91,12 +91,27 @@ int fill_and_launch(bool fused, const mxfp8_desc* d, const mxfp8_residual* res, 
         // beyond that (C = 32768: 74 % -> 83 % of HBM bandwidth); the residual
         // form, whose re-read is of h, does better with the larger cluster at
         // once (16384: +2.7 %).
+        //
+        // A launch whose CTAs at that size would not fill the device once
+        // (fewer than it holds at a time) is bound by the latency of its
+        // passes, not by bandwidth: it takes one pass per CTA instead, in
+        // larger clusters (256 x 1024: 11.1 -> 9.3 us, 64 x 8192: 14.8 ->
+        // 10.7 us, 16384 x 1024: 25.1 -> 23.2 us with the L2 flushed; raising
+        // the threshold to two or more device fills slowed 8192 x 4096 and
+        // 8192 x 8192 by 4-10 %).
         constexpr int64_t kWideSlicePasses = 4;
         const int64_t chunk = mx::fused_chunk_cols();
         int64_t want = ceil_div(max_cols, chunk * mx::kTargetChunks);
         if (want > mx::kPortableCluster && res == nullptr) {
             const int64_t wide = ceil_div(max_cols, chunk * kWideSlicePasses);
             want = wide > mx::kPortableCluster ? wide : mx::kPortableCluster;
+        }
+        int64_t stripes = 0;
+        for (int i = 0; i < n; ++i)
+            if (d[i].rows > 0 && d[i].cols > 0) stripes += ceil_div(d[i].rows, mx::kBlock);
+        if (stripes * want < mx::fused_resident_ctas()) {
+            const int64_t one_pass = ceil_div(max_cols, chunk);
+            if (one_pass > want) want = one_pass;
         }
         int most = mx::fused_max_cluster();
         const int cap = mx::hook_max_cluster();

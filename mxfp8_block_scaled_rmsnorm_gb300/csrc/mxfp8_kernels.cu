@@ -955,6 +955,28 @@ int bounds_status(bool clear, unsigned long long* out) {
 #endif
 }
 
+int fused_resident_ctas() {
+    constexpr int kMaxDevices = 64;
+    static int cache[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (dev >= 0 && dev < kMaxDevices && cache[dev] > 0) return cache[dev];
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, fused_rmsnorm_quant_kernel<kLargeTable, false, false>, FusedGeo::kThreads,
+            0) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    const int n = sms * per_sm;
+    if (dev >= 0 && dev < kMaxDevices) cache[dev] = n;
+    return n;
+}
+
 int fused_max_cluster() {
     constexpr int kMaxDevices = 64;
     static int cache[kMaxDevices] = {0};
