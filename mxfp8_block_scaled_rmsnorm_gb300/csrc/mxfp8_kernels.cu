@@ -459,7 +459,28 @@ __device__ __forceinline__ void emit_planes(const uint4 (&y)[G::kRows], TileMax<
     }
     int64_t rp;
     uint8_t* sr = row_scale_base(s_row, at, at.col / kBlock, C / kBlock, rp);
-    const bool writes_row_scale = do_row && (g & 3) == 0;
+    if (do_row) {
+        // After the reduction all 4 lanes of a block hold its maxima of all
+        // the thread's rows, so lane i of the 4 stores the scale bytes of rows
+        // 4i .. 4i + 3: four stores per tile with every lane active, where one
+        // lane in four storing all 16 rows took sixteen (128 ragged tensors:
+        // 674 -> 668 us with compact scales, 680 -> 660 us tiled).
+        const int i4 = g & 3;
+        uint32_t lo = 0, hi = 0;  // scale bytes of rows 4 i4, +1 (bits 0-7, 16-23); +2, +3
+#pragma unroll
+        for (int j = 0; j < kR / 2; ++j) {
+            if (j == 2 * i4) lo = rbytes[j];
+            if (j == 2 * i4 + 1) hi = rbytes[j];
+        }
+        uint8_t* sl = sr + (4 * i4) * rp;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const uint32_t w = t < 2 ? lo : hi;
+            if ((FULL || 4 * i4 + t < at.nrows) &&
+                MX_IN((sl - s_row) + t * rp, 1, srow_extent(at), kSiteSRow))
+                sl[t * rp] = (uint8_t)((t & 1) ? (w >> 16) : w);
+        }
+    }
     const bool lines = (C & 127) == 0;  // code rows start on 128-byte lines
 #pragma unroll
     for (int i = 0; i < kR; ++i) {
@@ -474,8 +495,6 @@ __device__ __forceinline__ void emit_planes(const uint4 (&y)[G::kRows], TileMax<
                 st_code8(reinterpret_cast<uint2*>(q_row + base + i * C),
                        make_uint2(e4m3x4(mul2(p0, ss), mul2(p1, ss)),
                                   e4m3x4(mul2(p2, ss), mul2(p3, ss))), lines);
-            if (writes_row_scale && MX_IN((sr - s_row) + i * rp, 1, srow_extent(at), kSiteSRow))
-                sr[i * rp] = (uint8_t)byte;
         }
         if (do_col && MX_IN(base + i * C, 8, at.rows * C, kSiteQCol))
             st_code8(reinterpret_cast<uint2*>(q_col + base + i * C),
