@@ -108,6 +108,19 @@ def test_fused_both_planes_shapes(R, C):
     check_fused(wl)
 
 
+@pytest.mark.parametrize("R,C", [(24576, 1056), (12288, 2080)])
+def test_fused_two_pass_slices_ragged_columns(R, C):
+    """Launches of more stripes than the device holds CTAs at once keep two
+    512-column passes per CTA (smaller ones take one pass per CTA in larger
+    clusters, which the shapes above cover); here with slices that end in a
+    partial pass (C = 1056: two CTAs of 544 columns; 2080: three of 704).
+    Checked on whole 32-row stripes at the start, middle and end."""
+    wl = W.random_fused(R, C, seed=R + C, eps=1e-6, offset=0.5)
+    mid = R // 2 - (R // 2) % 32
+    rows = np.concatenate([np.arange(0, 64), np.arange(mid, mid + 64), np.arange(R - 64, R)])
+    check_fused(wl, rows_sample=rows)
+
+
 @pytest.mark.parametrize("rowwise,columnwise", [(True, False), (False, True)])
 def test_fused_single_plane(rowwise, columnwise):
     wl = W.random_fused(64, 2048, seed=5, scale=4.0)
