@@ -42,7 +42,9 @@ def test_quant_mma_scales_match_oracle(R, C):
     assert np.array_equal(u8(got.s_col).ravel(), oracle.scales_to_mma(s_col, columnwise=True))
 
 
-@pytest.mark.parametrize("R,C", SHAPES)
+# 24576 x 1056: more stripes than the device holds CTAs at once, so the
+# two-pass slices (two CTAs of 544 columns) rather than one pass per CTA
+@pytest.mark.parametrize("R,C", SHAPES + [(24576, 1056)])
 def test_fused_mma_scales_match_compact_call(R, C):
     wl = W.random_fused(R, C, seed=3 * R + C, eps=1e-5, offset=0.5)
     t = wl.tensors[0]

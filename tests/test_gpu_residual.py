@@ -45,10 +45,12 @@ def _check(t, r_bits, h_dev, o, rowwise=True, columnwise=True):
             assert torch.equal(a, b), name
 
 
-# (64, 20480): 8-CTA clusters of 2560 columns, several passes per CTA
-# through the residual staging buffer
+# Small launches take one pass per CTA in clusters of up to 16 (64 x 20480:
+# 16 CTAs of 1280 columns, three passes each through the residual staging
+# buffer); 24576 x 1056 is more stripes than the device holds CTAs at once,
+# so two CTAs of 544 columns take two passes each, the second partial.
 @pytest.mark.parametrize("R,C", [(32, 32), (64, 1024), (96, 2080), (32, 8192), (64, 9216),
-                                 (256, 4096), (64, 20480)])
+                                 (256, 4096), (64, 20480), (24576, 1056)])
 def test_residual_add_shapes(R, C):
     t = W.random_fused(R, C, seed=R + 5 * C, eps=1e-5, offset=0.25).tensors[0]
     r = _residual((R, C), seed=R * C + 1, scale=0.5)
