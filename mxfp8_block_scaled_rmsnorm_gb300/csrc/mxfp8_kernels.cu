@@ -764,7 +764,14 @@ fused_rmsnorm_quant_kernel(const __grid_constant__ Table<MAXN> T) {
         part[tid] = s;
     }
     if (K > 1) {
-        cluster_arrive_release();
+        // only warp 0 wrote `part`: its arrival releases those writes to the
+        // peers; the other warps arrive without a release, which would wait
+        // for their own memory operations to complete (measured 1.8 % of a
+        // launch at 32768 x 8192)
+        if (warp == 0)
+            cluster_arrive_release();
+        else
+            asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
         cluster_wait_acquire();
         if (tid < kBlock) {
             // every peer's partial in flight at once, then added in rank order
