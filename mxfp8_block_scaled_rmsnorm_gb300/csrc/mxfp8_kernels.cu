@@ -29,12 +29,14 @@
 //    shuffles. A columnwise block (32 rows) spans the kGroups row groups of
 //    a warp: per-thread column maxima plus log2(kGroups) xor shuffles.
 //  - Fused kernel: a 32-row stripe of C columns is split over a thread-block
-//    cluster of K = ceil(C / 1024) CTAs (at most 8). Row partial sums of
-//    squares meet in each CTA's shared memory and are summed across the
-//    cluster through distributed shared memory, in rank order, so every CTA
-//    derives the same 1/rms for a row. A CTA's slice is kTargetChunks
-//    512-column passes wide when the row allows: after the row sums, the last
-//    pass is still in registers and the earlier ones are read again from L2.
+//    cluster of K CTAs (ceil(C / 1024) up to 8, up to 16 for wider rows
+//    where the device allows; launches too small to fill the device once
+//    take one 512-column pass per CTA instead). Row partial sums of squares
+//    meet in each CTA's shared memory and are summed across the cluster
+//    through distributed shared memory, in rank order, so every CTA derives
+//    the same 1/rms for a row. A CTA's slice is kTargetChunks 512-column
+//    passes wide when the row allows: after the row sums, the last pass is
+//    still in registers and the earlier ones are read again from L2.
 //  - L2 policy: outputs are written with streaming (evict-first) stores, so
 //    the pass-2 re-reads hit L2 and x crosses DRAM once; a residual input is
 //    staged per pass in shared memory by cp.async (evict-first) while x loads
@@ -50,7 +52,7 @@
 //    matter; products below 2^-126 quantize to a signed zero either way). The
 //    fused kernel forms it with fma.rn.f32.bf16 and the scale kept as bf16
 //    (quantize_tile: fewer live registers, which keeps it at 64 registers and
-//    two CTAs per SM); the quantize kernel unpacks each bf16 pair once and
+//    four 256-thread CTAs per SM); the quantize kernel unpacks each bf16 pair once and
 //    multiplies it by float32 scale pairs with mul.rn.f32x2 for both planes
 //    (emit_planes: fewer instructions). Both give the same float32 value and
 //    the same E4M3 code for every input, so the fused planes are
