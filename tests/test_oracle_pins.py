@@ -552,3 +552,18 @@ def test_dequantize_matches_library_decode_and_mm_closed_form():
     x = oracle.bf16_round(np.repeat(np.ldexp(1.0, a)[:, None], K, 1))
     w = oracle.bf16_round(np.repeat(np.ldexp(1.0, b)[:, None], K, 1))
     assert np.array_equal(oracle.mm_mxfp8(x, w, threads=1), K * np.ldexp(1.0, a[:, None] + b[None, :]))
+
+
+def test_mm_closed_form_with_a_scale_per_block():
+    """Each 32-element block of x and w holds one power of two, different from
+    block to block, so every block quantizes exactly (code 1.0 times its own
+    scale) and x w^T = sum over blocks of 32 * 2^(a[m, k] + b[n, k]): a block
+    paired with the wrong scale or the wrong partner block changes the sum."""
+    rng = np.random.default_rng(8)
+    M, N, nk = 3, 4, 5
+    a = rng.integers(-20, 20, (M, nk))
+    b = rng.integers(-20, 20, (N, nk))
+    x = oracle.bf16_round(np.repeat(np.ldexp(1.0, a), 32, axis=1))
+    w = oracle.bf16_round(np.repeat(np.ldexp(1.0, b), 32, axis=1))
+    want = 32.0 * np.ldexp(1.0, a[:, None, :] + b[None, :, :]).sum(axis=2)
+    assert np.array_equal(oracle.mm_mxfp8(x, w, threads=1), want)
