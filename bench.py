@@ -810,8 +810,8 @@ def main():
             "value": value,
             "ms_per_step": ms_per_step,
             "pct_of_peak": 100.0 * achieved / peak,
-            # the same against GB300's nominal HBM3e figure (the benchmark spec's
-            # "~8 TB/s"); the roofline fraction uses the measured copy peak
+            # the same against GB300's nominal HBM3e figure (about 8 TB/s);
+            # the roofline fraction uses the measured copy peak
             "pct_of_nominal_peak": 100.0 * achieved / NOMINAL_HBM_GBS,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
